@@ -1,0 +1,192 @@
+/*
+ * moe_gb300.h -- C ABI of libmoe_gb300: the routed Mixture-of-Experts expert-MLP
+ * layer (forward and backward) on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "LigerCute -- native CUTLASS + NVSHMEM kernels" (the
+ * liger-cute-kernels 0.8.3 package README), sections "Overview" and
+ * "LigerMoE design" (Forward pass, Backward pass).  The expert MLP is SwiGLU:
+ *   f_e(x) = (silu(x W_gate[e]) * (x W_up[e])) W_down[e],  silu(z) = z / (1 + e^-z).
+ * The layer output is Y[t] = sum_k topk_w[t,k] * f_{topk_ids[t,k]}(x[t]).
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense and row-major.  bf16 tensors are passed as raw 16-bit
+ *     storage (moe_bf16_t).  Sizes are element counts.
+ *   - Device pointers point to memory of the current CUDA device.  The library
+ *     allocates nothing and never synchronises the host (except
+ *     moe_get_device_error and moe_timing_collect); every call enqueues its kernels
+ *     on `stream` (a cudaStream_t, NULL = legacy default stream) and returns.
+ *   - The caller owns every buffer.  Buffers must not alias unless stated.
+ *   - Arguments are validated on the host before anything is launched; a failed
+ *     check returns a negative moe_status_t and launches nothing.  Conditions only
+ *     the GPU can see (an expert id outside [0,E), a bounded wait that gave up) are
+ *     recorded in the first word of `workspace` and read with moe_get_device_error.
+ *   - Notation: T tokens, K experts per token, E experts, D hidden size,
+ *     I expert intermediate size, R = T*K routed slots, cap = moe_capacity(T,K,E,align).
+ *   - Entry points that run GEMMs (moe_expert_mlp_fwd / _bwd) need D % 256 == 0,
+ *     I % 128 == 0 and align % 128 == 0; every pointer they read through TMA must be
+ *     16-byte aligned.  Launch shapes depend only on sizes, never on the routing, so
+ *     a fixed-size call sequence can be captured once in a CUDA graph and replayed
+ *     with new routings.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef uint16_t moe_bf16_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* a size, pointer or alignment check failed */
+  MOE_ERR_UNSUPPORTED = -2,   /* not an sm_103 device, or a shape the kernels do not cover */
+  MOE_ERR_CUDA = -3,          /* a CUDA runtime / driver call failed */
+  MOE_ERR_DEVICE_TIMEOUT = -4,/* (device error word) a kernel's bounded wait gave up */
+  MOE_ERR_BAD_INDEX = -5      /* (device error word) an expert id outside [0, E) */
+} moe_status_t;
+
+/* Version of this ABI (MOE_ABI_VERSION). */
+int moe_abi_version(void);
+
+/* Static, human-readable text for a moe_status_t value. */
+const char* moe_status_string(int status);
+
+/*
+ * Rows of every expert-sorted ("perm") buffer: R + E*(align-1), rounded up to a
+ * multiple of `align`.  Sized from the total routed-token count rather than a
+ * per-expert capacity ("Overview": symmetric buffers sized from the total
+ * routed-token capacity keep execution CUDA-Graph compatible under dynamic
+ * routing).  Returns 0 for invalid arguments.
+ */
+size_t moe_capacity(int T, int K, int E, int align);
+
+/*
+ * Bytes of scratch the layer needs: a 1 KB header (device error word), routing
+ * chunk counters, the dW split schedule, the activation act [cap, I], the hidden
+ * gradient [cap, 2I] and the routed output gradient [cap, D] (bf16).  One
+ * workspace may serve the forward and the backward of the same sizes, but not
+ * two calls running concurrently.  Returns 0 for invalid arguments.
+ */
+size_t moe_workspace_bytes(int T, int K, int E, int D, int I, int align);
+
+/*
+ * Zeroes the workspace header (the device error word).  Call once after
+ * allocating a workspace.  Asynchronous on `stream`.
+ */
+int moe_workspace_init(void* workspace, void* stream);
+
+/*
+ * Expert sort ("LigerMoE design / Forward pass": routed tokens are sorted by
+ * expert before the main loop).  A slot is the flat index j = t*K + k.
+ *
+ *   topk_ids [T,K] int32 (device)  expert of each slot, in [0, E); a token may repeat an expert
+ *   topk_w   [T,K] fp32  (device)  router weight of each slot
+ *   x        [T,D] bf16  (device)  token activations; NULL skips the row gather
+ * Outputs (device):
+ *   counts   [E]     int32  slots per expert
+ *   offsets  [E+1]   int32  offsets[0] = 0, offsets[e+1] = offsets[e] + ceil(counts[e]/align)*align
+ *   perm_src [cap]   int32  the slot j stored at sorted row s; -1 on padding and beyond offsets[E]
+ *   inv_perm [R]     int32  sorted row of slot j (perm_src[inv_perm[j]] == j)
+ *   w_perm   [cap]   fp32   router weight at sorted row s; 0 on padding
+ *   x_perm   [cap,D] bf16   x[perm_src[s] / K] at sorted row s, zero rows on padding;
+ *                           rows at and beyond offsets[E] are not written (ignored if x is NULL)
+ * Within an expert, slots keep ascending j, so the result is unique and matches the
+ * oracle bit for bit.  Constraints: T >= 0, 1 <= K <= 32, 1 <= E <= 1024, align >= 1,
+ * D % 8 == 0 (when x is given), R and cap < 2^31.  Uses the workspace's routing counters.
+ */
+int moe_route_permute(const int32_t* topk_ids, const float* topk_w, const moe_bf16_t* x,
+                      int T, int K, int E, int D, int align,
+                      int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
+                      float* w_perm, moe_bf16_t* x_perm, void* workspace, void* stream);
+
+/*
+ * Expert MLP forward on the sorted rows ("LigerMoE design / Forward pass": the MMA
+ * warps execute the expert MLP).  For every row s of expert e (offsets[e] <= s < offsets[e+1]):
+ *   act[s]    = bf16( silu(x_perm[s] W_gate[e]) * (x_perm[s] W_up[e]) )   (fp32 accumulate)
+ *   y_perm[s] = bf16( act[s] W_down[e] )                                  (fp32 accumulate)
+ *   x_perm [cap,D] bf16, w_gate [E,D,I] bf16, w_up [E,D,I] bf16, w_down [E,I,D] bf16,
+ *   offsets [E+1] int32 (from moe_route_permute with the same align) -- all device.
+ *   y_perm [cap,D] bf16 (device): rows < offsets[E] written; padding rows come out zero.
+ * act is kept in the workspace.  Needs D % 256 == 0, I % 128 == 0, align % 128 == 0.
+ */
+int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_gate,
+                       const moe_bf16_t* w_up, const moe_bf16_t* w_down,
+                       const int32_t* offsets, int T, int K, int E, int D, int I, int align,
+                       moe_bf16_t* y_perm, void* workspace, void* stream);
+
+/*
+ * Token combine ("LigerMoE design": the forward's final local combine applies the
+ * router weights; the backward's final local dispatch reduces the routed dX back to
+ * the original tokens):
+ *   out[t] = bf16( sum_k w[t,k] * src_perm[inv_perm[t*K+k]] ),  fp32 sum, k ascending.
+ *   src_perm [rows,D] bf16, inv_perm [T*K] int32, topk_w [T,K] fp32 or NULL (weight 1),
+ *   out [T,D] bf16 -- all device; out must not alias src_perm.
+ * Constraints: T >= 0, 1 <= K <= 32, D % 8 == 0.
+ */
+int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float* topk_w,
+                int T, int K, int D, moe_bf16_t* out, void* stream);
+
+/*
+ * Expert MLP backward on the sorted rows ("LigerMoE design / Backward pass"):
+ *   1. routed expert-output gradient  dy_perm[s] = bf16(w_perm[s] * dy[perm_src[s] / K]) (0 on padding)
+ *   2. recompute G = x_perm W_gate[e], U = x_perm W_up[e]; dA = dy_perm W_down[e]^T;
+ *      act = silu(G) U, dG = dA U silu'(G), dU = dA silu(G)   (bf16, in the workspace)
+ *   3. input gradient  dx_perm[s] = bf16( dG[s] W_gate[e]^T + dU[s] W_up[e]^T )
+ *   4. weight gradients (fp32), accumulated over all of the expert's rows; experts with
+ *      more than 2048 rows are split and the parts are TMA reduce-added:
+ *        dw_down[e] = act_e^T dy_perm_e,  dw_gate[e] = x_perm_e^T dG_e,  dw_up[e] = x_perm_e^T dU_e
+ *      Experts with no rows get exactly zero.
+ *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets from moe_route_permute, weights as in
+ *   the forward -- all device.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
+ *   dw_gate [E,D,I] fp32, dw_up [E,D,I] fp32, dw_down [E,I,D] fp32 (fully overwritten).
+ * Reduce dx_perm to tokens with moe_combine(dx_perm, inv_perm, NULL, ...).
+ * Needs D % 256 == 0, I % 128 == 0, align % 128 == 0.
+ */
+int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm, const int32_t* perm_src,
+                       const float* w_perm, const int32_t* offsets,
+                       const moe_bf16_t* w_gate, const moe_bf16_t* w_up,
+                       const moe_bf16_t* w_down, int T, int K, int E, int D, int I, int align,
+                       moe_bf16_t* dx_perm, float* dw_gate, float* dw_up, float* dw_down,
+                       void* workspace, void* stream);
+
+/*
+ * Reads and clears the device error word of `workspace` (synchronises `stream`).
+ * *code receives MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT; *detail the
+ * raw device code (which role timed out).  For tests and debugging.
+ */
+int moe_get_device_error(void* workspace, int* code, int* detail, void* stream);
+
+/* ---- diagnostics ---------------------------------------------------------- */
+
+/* Number of distinct kernels; kernel ids are 0 .. moe_num_kernels()-1. */
+int moe_num_kernels(void);
+
+/* Static name of kernel `id`, or NULL. */
+const char* moe_kernel_name(int id);
+
+/* Kernels launched by this library since it was loaded (all ids; per id if counts != NULL,
+ * counts has moe_num_kernels() entries). */
+long long moe_launch_count(long long* counts);
+
+/*
+ * Per-kernel timing.  While enabled, every launch is bracketed by two CUDA events
+ * recorded on its own stream.  Not for use inside stream capture.
+ */
+int moe_timing_enable(int on);
+
+/* Waits for the recorded events, adds each launch's duration to ms[id] and 1 to
+ * launches[id] (arrays of moe_num_kernels() entries, zeroed by the caller), and
+ * forgets the records. */
+int moe_timing_collect(double* ms, long long* launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

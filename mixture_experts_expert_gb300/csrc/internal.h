@@ -1,0 +1,96 @@
+// Host-side declarations shared by the translation units of libmoe_gb300.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Device-side error codes written to the first word of the workspace.
+enum DevErr : int {
+  kDevOk = 0,
+  kDevBadExpertId = 1,      // a topk id outside [0, E)
+  kDevTimeoutProducer = 2,  // TMA producer gave up waiting on a free stage
+  kDevTimeoutMma = 3,       // MMA issuer gave up waiting on data or TMEM
+  kDevTimeoutEpilogue = 4,  // epilogue gave up waiting on an accumulator
+};
+
+// Identifiers of every kernel the library launches (for launch counting and timing).
+enum KernelId : int {
+  kKRouteCount = 0,
+  kKRouteScan,
+  kKRouteScatter,
+  kKGatherX,
+  kKGemmGateUp,
+  kKGemmDown,
+  kKCombine,
+  kKDispatchDy,
+  kKGemmBwdAct,
+  kKGemmDx,
+  kKDwPrep,
+  kKGemmDwGU,
+  kKGemmDwD,
+  kNumKernelIds
+};
+
+const char* kernel_name(int id);
+
+// Brackets one launch with timing events when timing is on; counts launches.
+struct LaunchScope {
+  LaunchScope(int id, cudaStream_t s);
+  ~LaunchScope();
+  int id;
+  cudaStream_t stream;
+  int slot;
+};
+
+// Grouped-GEMM variants (one tcgen05 kernel template, one instantiation each).
+enum class GemmKind : int { GateUp = 0, Down = 1, BwdAct = 2, Dx = 3, DwGU = 4, DwD = 5 };
+
+// Tile sizes shared by host and device.
+constexpr int kBM = 128;        // token rows (or feature rows for dW) per tile
+constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kDwChunkRows = 2048;  // tokens per dW split-K chunk
+
+struct GemmParams {
+  CUtensorMap mapA0;
+  CUtensorMap mapA1;
+  CUtensorMap mapB0;
+  CUtensorMap mapB1;
+  CUtensorMap mapB2;
+  CUtensorMap mapO0;
+  CUtensorMap mapO1;
+  CUtensorMap mapO2;
+  const int* offsets;      // [E+1] padded expert offsets (device)
+  const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
+  int* err;                // device error word
+  int E, D, I;
+  int n_tiles;             // N tiles per M tile
+  int m_tiles;             // M tiles per expert (dW kinds)
+};
+
+// Launch one grouped GEMM; `max_tiles` bounds the device-side tile count.
+template <GemmKind KIND>
+cudaError_t launch_gemm_kind(const GemmParams& p, int max_tiles, int num_sms, cudaStream_t s);
+
+// Route / movement kernels.
+cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, int T, int K,
+                         int E, int D, int align, int cap, int32_t* counts, int32_t* offsets,
+                         int32_t* perm_src, int32_t* inv_perm, float* w_perm, uint16_t* x_perm,
+                         int32_t* chunk_counts, int* err, cudaStream_t s);
+
+cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, const float* w_perm,
+                               const int32_t* offsets, int E, int K, int D, int cap,
+                               uint16_t* dst, int kernel_id, cudaStream_t s);
+
+cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
+                           int T, int K, int D, uint16_t* out, cudaStream_t s);
+
+cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float* dw_gate,
+                           float* dw_up, float* dw_down, int D, int I, cudaStream_t s);
+
+int route_num_chunks(int R);
+
+}  // namespace moe

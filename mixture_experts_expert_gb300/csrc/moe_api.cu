@@ -1,0 +1,466 @@
+// C ABI of libmoe_gb300: argument validation, workspace layout, TMA descriptor
+// encoding and the launch sequence of every entry point.  No allocation, no host
+// synchronisation on the compute path.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "moe_gb300.h"
+
+#define MOE_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+// ------------------------------------------------------------------ launch bookkeeping
+static const char* const kKernelNames[kNumKernelIds] = {
+    "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
+    "gemm_down",   "combine",    "dispatch_dy",   "gemm_bwd_act", "gemm_dx",
+    "dw_prep",     "gemm_dw_gateup", "gemm_dw_down"};
+
+const char* kernel_name(int id) {
+  return (id >= 0 && id < kNumKernelIds) ? kKernelNames[id] : nullptr;
+}
+
+namespace {
+std::atomic<long long> g_launch_total{0};
+std::atomic<long long> g_launch_by_id[kNumKernelIds];
+std::mutex g_timing_mu;
+bool g_timing = false;
+struct TimingRec {
+  int id;
+  cudaEvent_t a, b;
+};
+std::vector<TimingRec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+LaunchScope::LaunchScope(int id_, cudaStream_t s) : id(id_), stream(s), slot(-1) {
+  g_launch_total.fetch_add(1, std::memory_order_relaxed);
+  if (id >= 0 && id < kNumKernelIds) g_launch_by_id[id].fetch_add(1, std::memory_order_relaxed);
+  if (g_timing) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    TimingRec r{id, pool_event(), pool_event()};
+    cudaEventRecord(r.a, s);
+    g_recs.push_back(r);
+    slot = static_cast<int>(g_recs.size()) - 1;
+  }
+}
+
+LaunchScope::~LaunchScope() {
+  if (slot >= 0) {
+    std::lock_guard<std::mutex> lk(g_timing_mu);
+    cudaEventRecord(g_recs[slot].b, stream);
+  }
+}
+
+// ------------------------------------------------------------------ device facts
+struct DevFacts {
+  bool init = false;
+  int num_sms = 0;
+  int major = 0, minor = 0;
+};
+static DevFacts g_dev[64];
+static std::mutex g_dev_mu;
+
+static const DevFacts* dev_facts() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevFacts& f = g_dev[dev];
+  if (!f.init) {
+    if (cudaDeviceGetAttribute(&f.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    cudaDeviceGetAttribute(&f.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&f.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    f.init = true;
+  }
+  return &f;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [outer, inner] tensor with a box of [box_outer, box_inner].
+static bool make_map(CUtensorMap* m, bool f32, const void* base, uint64_t inner, uint64_t outer,
+                     uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t esize = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand load maps (128-byte swizzle, 64-element inner box) and store maps.
+static bool map_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows) {
+  return make_map(m, false, b, inner, outer, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+static bool map_mnmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return make_map(m, false, b, inner, outer, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+static bool map_store_bf16(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return make_map(m, false, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+static bool map_store_f32(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
+  return make_map(m, true, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// ------------------------------------------------------------------ sizes
+static bool basic_sizes_ok(int T, int K, int E, int align) {
+  if (T < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || align < 1) return false;
+  const long long R = static_cast<long long>(T) * K;
+  const long long cap = R + static_cast<long long>(E) * (align - 1) + align;
+  return R < (1ll << 31) && cap < (1ll << 31);
+}
+
+static size_t capacity_of(int T, int K, int E, int align) {
+  const size_t R = static_cast<size_t>(T) * K;
+  const size_t c = R + static_cast<size_t>(E) * (align - 1);
+  return (c + align - 1) / align * align;
+}
+
+static size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
+
+struct WsLayout {
+  size_t chunk_counts, dw_prefix, act, dh, dyp, total;
+};
+
+// header | routing chunk counters | dW split prefix | act | dH | dy_perm
+static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
+  WsLayout L;
+  const size_t cap = capacity_of(T, K, E, align);
+  const size_t nch = static_cast<size_t>(route_num_chunks(T * K));
+  size_t o = 1024;
+  L.chunk_counts = o;
+  o = up1k(o + static_cast<size_t>(E) * nch * 4);
+  L.dw_prefix = o;
+  o = up1k(o + static_cast<size_t>(E + 1) * 4);
+  L.act = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 2);
+  L.dh = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 4);
+  L.dyp = o;
+  o = up1k(o + cap * static_cast<size_t>(D) * 2);
+  L.total = o;
+  return L;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static int check_device() {
+  const DevFacts* f = dev_facts();
+  if (!f) return MOE_ERR_CUDA;
+  if (f->major != 10 || f->minor != 3) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+static bool gemm_shape_ok(int D, int I, int align) {
+  return D >= 256 && I >= 128 && D % 256 == 0 && I % 128 == 0 && align % 128 == 0 &&
+         static_cast<long long>(D) < (1ll << 24) && static_cast<long long>(I) < (1ll << 24);
+}
+
+static int to_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace moe
+
+using namespace moe;
+
+// ------------------------------------------------------------------ exported API
+MOE_EXPORT int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+MOE_EXPORT const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BAD_INDEX: return "expert id out of range";
+    default: return "unknown status";
+  }
+}
+
+MOE_EXPORT size_t moe_capacity(int T, int K, int E, int align) {
+  if (!basic_sizes_ok(T, K, E, align)) return 0;
+  return capacity_of(T, K, E, align);
+}
+
+MOE_EXPORT size_t moe_workspace_bytes(int T, int K, int E, int D, int I, int align) {
+  if (!basic_sizes_ok(T, K, E, align) || D < 0 || I < 0) return 0;
+  return ws_layout(T, K, E, D, I, align).total;
+}
+
+MOE_EXPORT int moe_workspace_init(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  return to_status(cudaMemsetAsync(workspace, 0, 1024, static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_route_permute(const int32_t* topk_ids, const float* topk_w,
+                                 const moe_bf16_t* x, int T, int K, int E, int D, int align,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                                 int32_t* inv_perm, float* w_perm, moe_bf16_t* x_perm,
+                                 void* workspace, void* stream) {
+  if (!basic_sizes_ok(T, K, E, align)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || !perm_src || !w_perm || !workspace) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !topk_w || !inv_perm)) return MOE_ERR_INVALID_ARG;
+  if (x && (!x_perm || D <= 0 || D % 8 != 0 || !aligned16(x) || !aligned16(x_perm)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  const WsLayout L = ws_layout(T, K, E, D > 0 ? D : 0, 0, align);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int cap = static_cast<int>(capacity_of(T, K, E, align));
+  return to_status(launch_route(topk_ids, topk_w, x, T, K, E, D, align, cap, counts, offsets,
+                                perm_src, inv_perm, w_perm, x_perm,
+                                reinterpret_cast<int32_t*>(ws + L.chunk_counts),
+                                reinterpret_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm,
+                           const float* topk_w, int T, int K, int D, moe_bf16_t* out,
+                           void* stream) {
+  if (T < 0 || K < 1 || K > 32 || D <= 0 || D % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!src_perm || !inv_perm || !out)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(src_perm) || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  return to_status(launch_combine(src_perm, inv_perm, topk_w, T, K, D, out,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_gate,
+                                  const moe_bf16_t* w_up, const moe_bf16_t* w_down,
+                                  const int32_t* offsets, int T, int K, int E, int D, int I,
+                                  int align, moe_bf16_t* y_perm, void* workspace, void* stream) {
+  if (!basic_sizes_ok(T, K, E, align)) return MOE_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(D, I, align)) return MOE_ERR_UNSUPPORTED;
+  if (!x_perm || !w_gate || !w_up || !w_down || !offsets || !y_perm || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(y_perm) || !aligned16(workspace))
+    return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  const DevFacts* f = dev_facts();
+  const WsLayout L = ws_layout(T, K, E, D, I, align);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint64_t cap = capacity_of(T, K, E, align);
+  void* act = ws + L.act;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int m_tiles_max = static_cast<int>(cap / kBM);
+
+  GemmParams p{};
+  p.offsets = offsets;
+  p.err = reinterpret_cast<int*>(ws);
+  p.E = E; p.D = D; p.I = I;
+  // gate/up + SwiGLU
+  bool ok = map_kmajor(&p.mapA0, x_perm, D, cap, 128) &&
+            map_mnmajor(&p.mapB0, w_gate, I, static_cast<uint64_t>(E) * D) &&
+            map_mnmajor(&p.mapB1, w_up, I, static_cast<uint64_t>(E) * D) &&
+            map_store_bf16(&p.mapO0, act, I, cap);
+  if (!ok) return MOE_ERR_CUDA;
+  p.n_tiles = I / 128;
+  cudaError_t e;
+  {
+    LaunchScope ls(kKGemmGateUp, s);
+    e = launch_gemm_kind<GemmKind::GateUp>(p, m_tiles_max * p.n_tiles, f->num_sms, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // down projection
+  GemmParams q{};
+  q.offsets = offsets;
+  q.err = p.err;
+  q.E = E; q.D = D; q.I = I;
+  ok = map_kmajor(&q.mapA0, act, I, cap, 128) &&
+       map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I) &&
+       map_store_bf16(&q.mapO0, y_perm, D, cap);
+  if (!ok) return MOE_ERR_CUDA;
+  q.n_tiles = D / 256;
+  {
+    LaunchScope ls(kKGemmDown, s);
+    e = launch_gemm_kind<GemmKind::Down>(q, m_tiles_max * q.n_tiles, f->num_sms, s);
+  }
+  return to_status(e);
+}
+
+MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm,
+                                  const int32_t* perm_src, const float* w_perm,
+                                  const int32_t* offsets, const moe_bf16_t* w_gate,
+                                  const moe_bf16_t* w_up, const moe_bf16_t* w_down, int T, int K,
+                                  int E, int D, int I, int align, moe_bf16_t* dx_perm,
+                                  float* dw_gate, float* dw_up, float* dw_down, void* workspace,
+                                  void* stream) {
+  if (!basic_sizes_ok(T, K, E, align)) return MOE_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(D, I, align)) return MOE_ERR_UNSUPPORTED;
+  if (!x_perm || !perm_src || !w_perm || !offsets || !w_gate || !w_up || !w_down || !dx_perm ||
+      !dw_gate || !dw_up || !dw_down || !workspace || (T > 0 && !dy))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(dx_perm) || !aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down) ||
+      !aligned16(workspace) || (dy && !aligned16(dy)))
+    return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  const DevFacts* f = dev_facts();
+  const WsLayout L = ws_layout(T, K, E, D, I, align);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint64_t cap = capacity_of(T, K, E, align);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* err = reinterpret_cast<int*>(ws);
+  void* act = ws + L.act;
+  void* dh = ws + L.dh;
+  moe_bf16_t* dyp = reinterpret_cast<moe_bf16_t*>(ws + L.dyp);
+  int* dw_prefix = reinterpret_cast<int*>(ws + L.dw_prefix);
+  const int m_tiles_max = static_cast<int>(cap / kBM);
+  const uint64_t ED = static_cast<uint64_t>(E) * D, EI = static_cast<uint64_t>(E) * I;
+  cudaError_t e;
+
+  // 1. routed expert-output gradient
+  e = launch_gather_rows(dy, perm_src, w_perm, offsets, E, K, D, static_cast<int>(cap), dyp,
+                         kKDispatchDy, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 2. recompute + dA + SwiGLU'
+  GemmParams a{};
+  a.offsets = offsets; a.err = err; a.E = E; a.D = D; a.I = I;
+  bool ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) && map_kmajor(&a.mapA1, dyp, D, cap, 128) &&
+            map_mnmajor(&a.mapB0, w_gate, I, ED) && map_mnmajor(&a.mapB1, w_up, I, ED) &&
+            map_kmajor(&a.mapB2, w_down, D, EI, 128) && map_store_bf16(&a.mapO0, act, I, cap) &&
+            map_store_bf16(&a.mapO1, dh, 2ull * I, cap);
+  if (!ok) return MOE_ERR_CUDA;
+  a.n_tiles = I / 128;
+  {
+    LaunchScope ls(kKGemmBwdAct, s);
+    e = launch_gemm_kind<GemmKind::BwdAct>(a, m_tiles_max * a.n_tiles, f->num_sms, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 3. input gradient
+  GemmParams x{};
+  x.offsets = offsets; x.err = err; x.E = E; x.D = D; x.I = I;
+  ok = map_kmajor(&x.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&x.mapB0, w_gate, I, ED, 256) &&
+       map_kmajor(&x.mapB1, w_up, I, ED, 256) && map_store_bf16(&x.mapO0, dx_perm, D, cap);
+  if (!ok) return MOE_ERR_CUDA;
+  x.n_tiles = D / 256;
+  {
+    LaunchScope ls(kKGemmDx, s);
+    e = launch_gemm_kind<GemmKind::Dx>(x, m_tiles_max * x.n_tiles, f->num_sms, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 4. weight gradients
+  e = launch_dw_prep(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int max_chunks = E + static_cast<int>(cap / kDwChunkRows) + 1;
+  GemmParams g{};
+  g.offsets = offsets; g.dw_prefix = dw_prefix; g.err = err; g.E = E; g.D = D; g.I = I;
+  ok = map_mnmajor(&g.mapA0, x_perm, D, cap) && map_mnmajor(&g.mapB0, dh, 2ull * I, cap) &&
+       map_store_f32(&g.mapO0, dw_gate, I, ED) && map_store_f32(&g.mapO1, dw_up, I, ED);
+  if (!ok) return MOE_ERR_CUDA;
+  g.m_tiles = D / 128;
+  g.n_tiles = (2 * I) / 256;
+  {
+    LaunchScope ls(kKGemmDwGU, s);
+    e = launch_gemm_kind<GemmKind::DwGU>(g, max_chunks * g.m_tiles * g.n_tiles, f->num_sms, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  GemmParams d{};
+  d.offsets = offsets; d.dw_prefix = dw_prefix; d.err = err; d.E = E; d.D = D; d.I = I;
+  ok = map_mnmajor(&d.mapA0, act, I, cap) && map_mnmajor(&d.mapB0, dyp, D, cap) &&
+       map_store_f32(&d.mapO0, dw_down, D, EI);
+  if (!ok) return MOE_ERR_CUDA;
+  d.m_tiles = I / 128;
+  d.n_tiles = D / 256;
+  {
+    LaunchScope ls(kKGemmDwD, s);
+    e = launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, f->num_sms, s);
+  }
+  return to_status(e);
+}
+
+MOE_EXPORT int moe_get_device_error(void* workspace, int* code, int* detail, void* stream) {
+  if (!workspace || !code) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int raw = 0;
+  if (cudaMemcpyAsync(&raw, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = raw;
+  if (raw == kDevOk) *code = MOE_OK;
+  else if (raw == kDevBadExpertId) *code = MOE_ERR_BAD_INDEX;
+  else *code = MOE_ERR_DEVICE_TIMEOUT;
+  if (raw != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_num_kernels(void) { return kNumKernelIds; }
+
+MOE_EXPORT const char* moe_kernel_name(int id) { return kernel_name(id); }
+
+MOE_EXPORT long long moe_launch_count(long long* counts) {
+  if (counts)
+    for (int i = 0; i < kNumKernelIds; ++i) counts[i] = g_launch_by_id[i].load();
+  return g_launch_total.load();
+}
+
+MOE_EXPORT int moe_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  g_timing = on != 0;
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_timing_collect(double* ms, long long* launches) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  int status = MOE_OK;
+  for (auto& r : g_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) {
+      status = MOE_ERR_CUDA;
+    } else if (r.id >= 0 && r.id < kNumKernelIds) {
+      if (ms) ms[r.id] += t;
+      if (launches) launches[r.id] += 1;
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  return status;
+}

@@ -1,0 +1,338 @@
+// Routing and data-movement kernels (HBM-bound): expert histogram, prefix scan,
+// stable scatter into expert-sorted order, row gather (x and the router-weighted
+// dY), the weighted combine back to tokens, and the dW split-K preparation.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kChunk = 256;           // flat routed slots per chunk (one warp each)
+constexpr int kRouteWarps = 8;        // warps per block in the count / scatter kernels
+
+int route_num_chunks(int R) { return (R + kChunk - 1) / kChunk; }
+
+// Per-chunk expert histogram into chunk_counts[e][c]; also marks every sorted row as
+// padding (perm_src = -1, w_perm = 0) before the scatter fills the real ones.
+__global__ void __launch_bounds__(kRouteWarps * 32) k_route_count(
+    const int32_t* __restrict__ ids, int R, int E, int nchunks, int cap,
+    int32_t* __restrict__ chunk_counts, int32_t* __restrict__ perm_src,
+    float* __restrict__ w_perm, int* err) {
+  extern __shared__ int sh_hist[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < cap; i += gridDim.x * blockDim.x) {
+    perm_src[i] = -1;
+    w_perm[i] = 0.f;
+  }
+  int* h = sh_hist + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int c = blockIdx.x * kRouteWarps + warp;
+  if (c >= nchunks) return;
+  for (int i = lane; i < kChunk; i += 32) {
+    const int j = c * kChunk + i;
+    if (j < R) {
+      const int e = __ldg(ids + j);
+      if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&h[e], 1);
+      else report_error(err, kDevBadExpertId);
+    }
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) chunk_counts[static_cast<size_t>(e) * nchunks + c] = h[e];
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// One 1024-thread block: per expert, exclusive prefix over chunks (in place, giving each
+// chunk's first rank inside the expert); the expert counts; the padded offsets.
+__global__ void __launch_bounds__(1024) k_route_scan(int E, int nchunks, int align,
+                                                     int32_t* __restrict__ chunk_counts,
+                                                     int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ offsets) {
+  __shared__ int s_cnt[1024];
+  __shared__ int s_warp[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = warp; e < E; e += 32) {
+    int32_t* row = chunk_counts + static_cast<size_t>(e) * nchunks;
+    int running = 0;
+    for (int cb = 0; cb < nchunks; cb += 32) {
+      const int c = cb + lane;
+      const int v = c < nchunks ? row[c] : 0;
+      const int incl = warp_incl_scan(v, lane);
+      if (c < nchunks) row[c] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_cnt[e] = running;
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int cnt = e < E ? s_cnt[e] : 0;
+  const int pad = (cnt + align - 1) / align * align;
+  const int incl = warp_incl_scan(pad, lane);
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = s_warp[lane];
+    const int wi = warp_incl_scan(v, lane);
+    s_warp[lane] = wi - v;
+  }
+  __syncthreads();
+  const int excl = s_warp[warp] + incl - pad;
+  if (e < E) {
+    counts[e] = cnt;
+    offsets[e] = excl;
+  }
+  if (e == E - 1) offsets[E] = excl + pad;
+}
+
+// Stable scatter: each warp walks its chunk in slot order; equal experts inside a
+// 32-slot step are ranked by lane, and a per-warp running row per expert carries the
+// order across steps.  Slot j lands on row offsets[e] + (rank of j among e's slots).
+__global__ void __launch_bounds__(kRouteWarps * 32) k_route_scatter(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int R, int E, int nchunks,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+    int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
+    float* __restrict__ w_perm) {
+  extern __shared__ int sh_run[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kRouteWarps + warp;
+  if (c >= nchunks) return;
+  int* run = sh_run + warp * E;
+  for (int e = lane; e < E; e += 32)
+    run[e] = __ldg(offsets + e) + chunk_base[static_cast<size_t>(e) * nchunks + c];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int it = 0; it < kChunk / 32; ++it) {
+    const int j = c * kChunk + it * 32 + lane;
+    int e = j < R ? __ldg(ids + j) : -1;
+    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    const int s = e >= 0 ? run[e] + rank : 0;
+    __syncwarp();
+    if (e >= 0 && rank == 0) run[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      perm_src[s] = j;
+      inv_perm[j] = s;
+      w_perm[s] = __ldg(w + j);
+    }
+  }
+}
+
+cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, int T, int K,
+                         int E, int D, int align, int cap, int32_t* counts, int32_t* offsets,
+                         int32_t* perm_src, int32_t* inv_perm, float* w_perm, uint16_t* x_perm,
+                         int32_t* chunk_counts, int* err, cudaStream_t s) {
+  const int R = T * K;
+  const int nchunks = route_num_chunks(R);
+  const int blocks = nchunks > 0 ? (nchunks + kRouteWarps - 1) / kRouteWarps : 1;
+  const size_t sh = static_cast<size_t>(kRouteWarps) * E * sizeof(int);
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaFuncSetAttribute(k_route_count, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    cudaFuncSetAttribute(k_route_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    configured[dev] = true;
+  }
+  {
+    LaunchScope ls(kKRouteCount, s);
+    k_route_count<<<blocks, kRouteWarps * 32, sh, s>>>(ids, R, E, nchunks, cap, chunk_counts,
+                                                       perm_src, w_perm, err);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    LaunchScope ls(kKRouteScan, s);
+    k_route_scan<<<1, 1024, 0, s>>>(E, nchunks, align, chunk_counts, counts, offsets);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (nchunks > 0) {
+    LaunchScope ls(kKRouteScatter, s);
+    k_route_scatter<<<blocks, kRouteWarps * 32, sh, s>>>(ids, w, R, E, nchunks, chunk_counts,
+                                                         offsets, perm_src, inv_perm, w_perm);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (x != nullptr) {
+    e = launch_gather_rows(x, perm_src, nullptr, offsets, E, K, D, cap, x_perm, kKGatherX, s);
+  }
+  return e;
+}
+
+// ------------------------------------------------------------------ row gather
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 q, float sc) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&w[i]);
+    const float2 f = __bfloat1622float2(b);
+    w[i] = pack_bf16x2(f.x * sc, f.y * sc);
+  }
+  return q;
+}
+
+// dst[s] = src[perm_src[s] / K] (times w_perm[s] when SCALE), zero on padding rows,
+// for s < offsets[E].  One warp per sorted row, 16-byte vectors.
+template <bool SCALE>
+__global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict__ src,
+                                                     const int32_t* __restrict__ perm_src,
+                                                     const float* __restrict__ w_perm,
+                                                     const int32_t* __restrict__ offsets, int E,
+                                                     int K, int D, uint16_t* __restrict__ dst) {
+  const int rows = __ldg(offsets + E);
+  const int lane = threadIdx.x & 31;
+  const int nvec = D >> 3;
+  const int wpg = (gridDim.x * blockDim.x) >> 5;
+  for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < rows; s += wpg) {
+    const int j = __ldg(perm_src + s);
+    uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(s) * D);
+    if (j < 0) {
+      for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* sp = reinterpret_cast<const uint4*>(src + static_cast<size_t>(j / K) * D);
+    const float sc = SCALE ? __ldg(w_perm + s) : 1.0f;
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      uint4 q0 = __ldg(sp + v), q1 = __ldg(sp + v + 32), q2 = __ldg(sp + v + 64),
+            q3 = __ldg(sp + v + 96);
+      if (SCALE) {
+        q0 = scale_bf16x8(q0, sc); q1 = scale_bf16x8(q1, sc);
+        q2 = scale_bf16x8(q2, sc); q3 = scale_bf16x8(q3, sc);
+      }
+      d[v] = q0; d[v + 32] = q1; d[v + 64] = q2; d[v + 96] = q3;
+    }
+    for (; v < nvec; v += 32) {
+      uint4 q = __ldg(sp + v);
+      if (SCALE) q = scale_bf16x8(q, sc);
+      d[v] = q;
+    }
+  }
+}
+
+cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, const float* w_perm,
+                               const int32_t* offsets, int E, int K, int D, int cap,
+                               uint16_t* dst, int kernel_id, cudaStream_t s) {
+  int blocks = (cap + 7) / 8;
+  if (blocks < 1) blocks = 1;
+  LaunchScope ls(kernel_id, s);
+  if (w_perm) k_gather_rows<true><<<blocks, 256, 0, s>>>(src, perm_src, w_perm, offsets, E, K, D, dst);
+  else k_gather_rows<false><<<blocks, 256, 0, s>>>(src, perm_src, nullptr, offsets, E, K, D, dst);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ combine
+// out[t] = sum_k w[t,k] * src[inv[t*K+k]] in fp32, k ascending, one warp per token.
+__global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ src,
+                                                 const int32_t* __restrict__ inv,
+                                                 const float* __restrict__ w, int T, int K,
+                                                 int D, uint16_t* __restrict__ out) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int my_row = lane < K ? __ldg(inv + static_cast<size_t>(t) * K + lane) : 0;
+  const float my_w = lane < K ? (w ? __ldg(w + static_cast<size_t>(t) * K + lane) : 1.0f) : 0.f;
+  const int nvec = D >> 3;
+  uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * D);
+  for (int v = lane; v < nvec; v += 32) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      uint4 q[8];
+      float wk[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u;
+        const int row = __shfl_sync(0xffffffffu, my_row, k & 31);
+        wk[u] = __shfl_sync(0xffffffffu, my_w, k & 31);
+        q[u] = k < K ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D) + v)
+                     : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (k0 + u >= K) break;
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(&q[u]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[i]));
+          acc[2 * i] = fmaf(wk[u], f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wk[u], f.y, acc[2 * i + 1]);
+        }
+      }
+    }
+    o[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
+                           int T, int K, int D, uint16_t* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + 7) / 8;
+  LaunchScope ls(kKCombine, s);
+  k_combine<<<blocks, 256, 0, s>>>(src_perm, inv_perm, w, T, K, D, out);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dW split-K preparation
+// Block 0 writes dw_prefix[e] = sum_{e' < e} chunks(e'), chunks(e) = max(1, ceil(rows_e / kDwChunkRows)).
+// Block e zeroes dW[e] when expert e is split (its tiles reduce-add into it).
+__global__ void __launch_bounds__(1024) k_dw_prep(const int32_t* __restrict__ offsets, int E,
+                                                  int* __restrict__ dw_prefix,
+                                                  float* __restrict__ dwg,
+                                                  float* __restrict__ dwu,
+                                                  float* __restrict__ dwd, int D, int I) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0) {
+    __shared__ int s_warp[32];
+    const int e = threadIdx.x;
+    int ch = 0;
+    if (e < E) {
+      const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
+      ch = (rows + kDwChunkRows - 1) / kDwChunkRows;
+      if (ch < 1) ch = 1;
+    }
+    const int incl = warp_incl_scan(ch, lane);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = s_warp[lane];
+      s_warp[lane] = warp_incl_scan(v, lane) - v;
+    }
+    __syncthreads();
+    const int excl = s_warp[warp] + incl - ch;
+    if (e < E) dw_prefix[e] = excl;
+    if (e == E - 1) dw_prefix[E] = excl + ch;
+  }
+  const int e = blockIdx.x;
+  if (e >= E) return;
+  const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
+  if (rows <= kDwChunkRows) return;
+  const size_t n4 = static_cast<size_t>(D) * I / 4;
+  float4* g4 = reinterpret_cast<float4*>(dwg + static_cast<size_t>(e) * D * I);
+  float4* u4 = reinterpret_cast<float4*>(dwu + static_cast<size_t>(e) * D * I);
+  float4* d4 = reinterpret_cast<float4*>(dwd + static_cast<size_t>(e) * D * I);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t i = threadIdx.x; i < n4; i += blockDim.x) {
+    g4[i] = z;
+    u4[i] = z;
+    d4[i] = z;
+  }
+}
+
+cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float* dw_gate,
+                           float* dw_up, float* dw_down, int D, int I, cudaStream_t s) {
+  LaunchScope ls(kKDwPrep, s);
+  k_dw_prep<<<E, 1024, 0, s>>>(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,69 @@
+"""A routed MoE expert-MLP layer of fixed size on one GPU: owns every buffer the
+C ABI needs (allocated once with torch, reused by every call) and strings the
+entry points together.
+
+Forward:  moe_route_permute -> moe_expert_mlp_fwd -> moe_combine(topk_w)
+Backward: moe_expert_mlp_bwd -> moe_combine(NULL)   (reduces routed dX to tokens)
+
+Buffer shapes are fixed by (T, K, E, D, I, align), so a forward/backward pair can
+be captured once in a CUDA graph and replayed with new inputs and routings.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class MoEExpertMLP:
+    def __init__(self, T: int, K: int, E: int, D: int, I: int, align: int = 128,
+                 device: str | torch.device = "cuda"):
+        self.T, self.K, self.E, self.D, self.I, self.align = T, K, E, D, I, align
+        dev = torch.device(device)
+        self.device = dev
+        self.cap = B.moe_capacity(T, K, E, align)
+        if self.cap == 0 and T * K > 0:
+            raise ValueError("invalid layer sizes")
+        cap = max(self.cap, 1)
+        i32, f32, bf = torch.int32, torch.float32, torch.bfloat16
+        self.counts = torch.zeros(E, dtype=i32, device=dev)
+        self.offsets = torch.zeros(E + 1, dtype=i32, device=dev)
+        self.perm_src = torch.empty(cap, dtype=i32, device=dev)
+        self.inv_perm = torch.empty(max(T * K, 1), dtype=i32, device=dev)
+        self.w_perm = torch.empty(cap, dtype=f32, device=dev)
+        self.x_perm = torch.empty(cap, D, dtype=bf, device=dev)
+        self.y_perm = torch.empty(cap, D, dtype=bf, device=dev)
+        self.y = torch.empty(T, D, dtype=bf, device=dev)
+        self.dx_perm = torch.empty(cap, D, dtype=bf, device=dev)
+        self.dx = torch.empty(T, D, dtype=bf, device=dev)
+        self.dw_gate = torch.empty(E, D, I, dtype=f32, device=dev)
+        self.dw_up = torch.empty(E, D, I, dtype=f32, device=dev)
+        self.dw_down = torch.empty(E, I, D, dtype=f32, device=dev)
+        ws = B.moe_workspace_bytes(T, K, E, D, I, align)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        B.moe_workspace_init(self.workspace)
+        self._topk_w = None
+
+    def forward(self, x, topk_ids, topk_w, w_gate, w_up, w_down, stream=None):
+        """Y [T, D] bf16 = sum_k topk_w[t,k] * SwiGLU-MLP_{topk_ids[t,k]}(x[t])."""
+        T, K, E, D, I, a = self.T, self.K, self.E, self.D, self.I, self.align
+        B.moe_route_permute(topk_ids, topk_w, x, T, K, E, D, a, self.counts, self.offsets,
+                            self.perm_src, self.inv_perm, self.w_perm, self.x_perm,
+                            self.workspace, stream)
+        B.moe_expert_mlp_fwd(self.x_perm, w_gate, w_up, w_down, self.offsets, T, K, E, D, I, a,
+                             self.y_perm, self.workspace, stream)
+        B.moe_combine(self.y_perm, self.inv_perm, topk_w, T, K, D, self.y, stream)
+        return self.y
+
+    def backward(self, dy, w_gate, w_up, w_down, stream=None):
+        """(dX [T,D] bf16, dW_gate [E,D,I] f32, dW_up [E,D,I] f32, dW_down [E,I,D] f32)
+        of L = sum(Y * dy), for the routing of the last forward."""
+        T, K, E, D, I, a = self.T, self.K, self.E, self.D, self.I, self.align
+        B.moe_expert_mlp_bwd(dy, self.x_perm, self.perm_src, self.w_perm, self.offsets, w_gate,
+                             w_up, w_down, T, K, E, D, I, a, self.dx_perm, self.dw_gate,
+                             self.dw_up, self.dw_down, self.workspace, stream)
+        B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, self.dx, stream)
+        return self.dx, self.dw_gate, self.dw_up, self.dw_down
+
+    def device_error(self, stream=None):
+        return B.moe_get_device_error(self.workspace, stream)

@@ -140,10 +140,12 @@ def expert_mlp_fwd(x_perm, w_gate, w_up, w_down, offsets, experts=None):
     For the rows s of expert e: G = x_perm[s] W_gate[e], U = x_perm[s] W_up[e],
     A = silu(G) * U, y_perm[s] = A W_down[e].  Padding rows are zero in, zero out.
     ``experts`` restricts the work to a subset; rows of other experts are NaN.
+    The weights may be indexable per expert (e.g. a list holding only the experts
+    that are computed).
     """
     x_perm = np.asarray(x_perm, dtype=np.float64)
     E = len(offsets) - 1
-    D = np.asarray(w_down).shape[2]
+    D = x_perm.shape[1]
     y = np.full((x_perm.shape[0], D), np.nan if experts is not None else 0.0)
     if experts is None:
         y[int(offsets[E]):] = 0.0
@@ -188,22 +190,26 @@ def expert_mlp_bwd(dy, x_perm, perm_src, w_perm, offsets, w_gate, w_up, w_down, 
       dx_perm[s] = dG W_gate[e]^T + dU W_up[e]^T     input gradient
       dW_down[e] = sum_s A^T dy_s,  dW_gate[e] = sum_s x_s^T dG,  dW_up[e] = sum_s x_s^T dU
     Padding rows carry zero gradient.  Experts with no rows get dW == 0.
-    ``experts`` restricts the work; dx_perm rows and dW of other experts are NaN.
+    ``experts`` restricts the work: dx_perm rows of other experts are NaN and the
+    three weight gradients come back as dicts {e: array} over the listed experts.
     """
     dy = np.asarray(dy, dtype=np.float64)
     x_perm = np.asarray(x_perm, dtype=np.float64)
     perm_src = np.asarray(perm_src, dtype=np.int64)
     w_perm = np.asarray(w_perm, dtype=np.float64)
     E = len(offsets) - 1
-    _, D, I = np.asarray(w_gate).shape
-    fill = np.nan if experts is not None else 0.0
-    dx_perm = np.full(x_perm.shape, fill)
-    dw_gate = np.full((E, D, I), fill)
-    dw_up = np.full((E, D, I), fill)
-    dw_down = np.full((E, I, D), fill)
+    todo = list(range(E) if experts is None else experts)
+    D = x_perm.shape[1]
+    I = np.asarray(w_gate[todo[0]]).shape[1] if todo else 0
     if experts is None:
-        dx_perm[int(offsets[E]):] = 0.0
-    for e in (range(E) if experts is None else experts):
+        dx_perm = np.zeros(x_perm.shape)
+        dw_gate = np.zeros((E, D, I))
+        dw_up = np.zeros((E, D, I))
+        dw_down = np.zeros((E, I, D))
+    else:
+        dx_perm = np.full(x_perm.shape, np.nan)
+        dw_gate, dw_up, dw_down = {}, {}, {}
+    for e in todo:
         rows = _expert_rows(offsets, e)
         src = perm_src[rows]
         real = src >= 0
@@ -238,8 +244,8 @@ def moe_forward(x, topk_ids, topk_w, w_gate, w_up, w_down):
     x = np.asarray(x, dtype=np.float64)
     ids = np.asarray(topk_ids, dtype=np.int64)
     w = np.asarray(topk_w, dtype=np.float64)
-    E = np.asarray(w_gate).shape[0]
-    y = np.zeros((x.shape[0], np.asarray(w_down).shape[2]))
+    E = len(w_gate)
+    y = np.zeros_like(x)
     for e in range(E):
         t, k = _tokens_of_expert(ids, e)
         if t.size == 0:
@@ -251,18 +257,18 @@ def moe_forward(x, topk_ids, topk_w, w_gate, w_up, w_down):
     return y
 
 
-def moe_backward(x, topk_ids, topk_w, w_gate, w_up, w_down, dy):
+def moe_backward(x, topk_ids, topk_w, w_gate, w_up, w_down, dy, weight_grads=True):
     """Gradients of L = sum(Y * dY) for the whole layer by its definition:
-    returns dX [T,D], dW_gate [E,D,I], dW_up [E,D,I], dW_down [E,I,D] (routing fixed)."""
+    returns dX [T,D], dW_gate [E,D,I], dW_up [E,D,I], dW_down [E,I,D] (routing fixed).
+    With ``weight_grads=False`` only dX is computed (the dW slots are None)."""
     x = np.asarray(x, dtype=np.float64)
     ids = np.asarray(topk_ids, dtype=np.int64)
     w = np.asarray(topk_w, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
-    E, D, I = np.asarray(w_gate).shape
+    E = len(w_gate)
+    D = x.shape[1]
     dx = np.zeros_like(x)
-    dwg = np.zeros((E, D, I))
-    dwu = np.zeros((E, D, I))
-    dwd = np.zeros((E, I, D))
+    dwg = dwu = dwd = None
     for e in range(E):
         t, k = _tokens_of_expert(ids, e)
         if t.size == 0:
@@ -279,7 +285,14 @@ def moe_backward(x, topk_ids, topk_w, w_gate, w_up, w_down, dy):
         dg = da * u * silu_grad(g)
         du = da * silu(g)
         np.add.at(dx, t, dg @ wg.T + du @ wu.T)
-        dwd[e] = a.T @ dys
-        dwg[e] = xe.T @ dg
-        dwu[e] = xe.T @ du
+        if weight_grads:
+            if dwg is None:
+                I = wg.shape[1]
+                dwg, dwu, dwd = np.zeros((E, D, I)), np.zeros((E, D, I)), np.zeros((E, I, D))
+            dwd[e] = a.T @ dys
+            dwg[e] = xe.T @ dg
+            dwu[e] = xe.T @ du
+    if weight_grads and dwg is None:   # no expert received a token
+        I = np.asarray(w_gate[0]).shape[1]
+        dwg, dwu, dwd = np.zeros((E, D, I)), np.zeros((E, D, I)), np.zeros((E, I, D))
     return dx, dwg, dwu, dwd

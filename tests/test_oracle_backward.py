@@ -139,6 +139,7 @@ def test_expert_subset_matches_full():
         assert np.array_equal(sub[0][rows], full[0][rows])
         for a, b in zip(sub[1:], full[1:]):
             assert np.array_equal(a[e], b[e])
+    assert sorted(sub[1]) == [1, 3]
     yf = oracle.expert_mlp_fwd(r["x_perm"], wg, wu, wd, r["offsets"])
     ys = oracle.expert_mlp_fwd(r["x_perm"], wg, wu, wd, r["offsets"], experts=[2])
     rows = slice(int(r["offsets"][2]), int(r["offsets"][3]))
