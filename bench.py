@@ -1,0 +1,385 @@
+"""Benchmark: routed MoE expert-MLP layer, forward + backward, on GB300.
+
+One step = the whole hot path on one batch of synthetic input already resident in
+HBM: moe_route_permute -> moe_expert_mlp_fwd -> moe_combine (Y) ->
+moe_expert_mlp_bwd -> moe_combine (dX).  FLOPs are counted algorithmically:
+forward 6*R*D*I, backward 12*R*D*I (R = T*K routed rows; the backward's
+activation recompute is not counted as work).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica of the layer on its own GPU (weak scaling, no collective).
+``--impl reference`` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE expert-MLP TFLOP/s fwd & bwd on 1 GB300 (% of BF16 dense peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ROOFLINE_KERNEL = "gemm_bwd_act"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen3_30b_a3b")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def get_shape(name):
+    from mixture_experts_expert_gb300 import synth
+    if name in synth.SHAPES:
+        return synth.SHAPES[name]
+    if name.startswith("qwen3_30b_a3b_T"):
+        return synth.sweep_shape(int(name.split("_T")[-1]))
+    raise SystemExit(f"unknown workload {name}")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(shape, budget_s=12.0):
+    """The oracle as it stands, on this host's cores, over a bounded sample: the
+    forward and backward of the first experts of the workload, expert by expert,
+    until the time budget is spent."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from mixture_experts_expert_gb300 import synth
+    s = shape
+    inp = synth.make_inputs(s)
+    x = inp["x"].double().numpy()
+    dy = inp["dy"].double().numpy()
+    ids = inp["topk_ids"].numpy().astype(np.int64)
+    w = inp["topk_w"].double().numpy()
+    r = oracle.route_permute(ids, w, x, s.E, 128)
+    wg = [inp["w_gate"][e].double().numpy() for e in range(s.E)]
+    wu = [inp["w_up"][e].double().numpy() for e in range(s.E)]
+    wd = [inp["w_down"][e].double().numpy() for e in range(s.E)]
+    done, rows, t0 = [], 0, time.perf_counter()
+    for e in range(s.E):
+        oracle.expert_mlp_fwd(r["x_perm"], wg, wu, wd, r["offsets"], experts=[e])
+        oracle.expert_mlp_bwd(dy, r["x_perm"], r["perm_src"], r["w_perm"], r["offsets"],
+                              wg, wu, wd, s.K, experts=[e])
+        done.append(e)
+        rows += int(r["counts"][e])
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 18.0 * rows * s.D * s.I
+    del torch
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"fp64 forward+backward of experts 0..{done[-1]} ({rows} routed rows of "
+                      f"{s.R}) of the {s.name} layer, {dt:.1f} s"}
+
+
+def run_reference(args, shape):
+    """The CPU oracle as the reference arm: each step is a bounded sample (one
+    expert's forward and backward), timed on the host cores."""
+    import numpy as np
+
+    import oracle
+    from mixture_experts_expert_gb300 import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    s = shape
+    inp = synth.make_inputs(s)
+    x = inp["x"].double().numpy()
+    dy = inp["dy"].double().numpy()
+    ids = inp["topk_ids"].numpy().astype(np.int64)
+    w = inp["topk_w"].double().numpy()
+    r = oracle.route_permute(ids, w, x, s.E, 128)
+    wg, wu, wd = (inp[k] for k in ("w_gate", "w_up", "w_down"))
+    lists = [[t[e].double().numpy() for e in range(s.E)] for t in (wg, wu, wd)]
+
+    def step(e):
+        oracle.expert_mlp_fwd(r["x_perm"], *lists, r["offsets"], experts=[e])
+        oracle.expert_mlp_bwd(dy, r["x_perm"], r["perm_src"], r["w_perm"], r["offsets"], *lists,
+                              s.K, experts=[e])
+        return int(r["counts"][e])
+
+    for i in range(args.warmup):
+        step(i % s.E)
+    rows, t0 = 0, time.perf_counter()
+    for i in range(args.steps):
+        rows += step((args.warmup + i) % s.E)
+    dt = time.perf_counter() - t0
+    value = 18.0 * rows * s.D * s.I / dt / 1e12
+    sample = (f"fp64 forward+backward of one expert per step ({rows} routed rows in "
+              f"{args.steps} steps) of the {s.name} layer")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": s.name, "T": s.T, "D": s.D, "I": s.I, "E": s.E, "K": s.K},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    shape = get_shape(args.workload)
+    if args.impl == "reference":
+        run_reference(args, shape)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import torch.distributed as dist
+
+    from mixture_experts_expert_gb300 import binding as B
+    from mixture_experts_expert_gb300 import build as Bld
+    from mixture_experts_expert_gb300 import synth
+    from mixture_experts_expert_gb300.layer import MoEExpertMLP
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        Bld.build()
+    if world > 1:
+        dist.barrier()
+    B.lib()
+
+    s = shape
+    inp = synth.make_inputs(s, device=dev)
+    layer = MoEExpertMLP(s.T, s.K, s.E, s.D, s.I, align=128, device=dev)
+    wg, wu, wd = inp["w_gate"], inp["w_up"], inp["w_down"]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.forward(inp["x"], inp["topk_ids"], inp["topk_w"], wg, wu, wd)
+        ev_mid.record(stream)
+        layer.backward(inp["dy"], wg, wu, wd)
+
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert layer.device_error()[0] == B.MOE_OK
+
+    # ---------------- timed region (device-resident inputs)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    B.moe_timing_collect()   # drop anything recorded before
+    launches0, _ = B.moe_launch_count()
+    B.moe_timing_enable(True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        starts[i].record(stream)
+        ev_mid = mids[i]
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    B.moe_timing_enable(False)
+    launches1, _ = B.moe_launch_count()
+    clocks = sampler.stop()
+    per_kernel = B.moe_timing_collect()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    fwd_ms = [a.elapsed_time(b) for a, b in zip(starts, mids)]
+    bwd_ms = [a.elapsed_time(b) for a, b in zip(mids, ends)]
+    total_ms = starts[0].elapsed_time(ends[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    step_flops = s.fwd_flops() + s.bwd_flops()
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    fwd_tflops = s.fwd_flops() / (statistics.median(fwd_ms) * 1e-3) / 1e12
+    bwd_tflops = s.bwd_flops() / (statistics.median(bwd_ms) * 1e-3) / 1e12
+
+    # ---------------- end to end through host buffers (pinned), same step
+    host = {k: inp[k].cpu().pin_memory() for k in ("x", "topk_ids", "topk_w", "dy")}
+    out_y = torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory()
+    out_dx = torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_y.numel() * out_y.element_size() + out_dx.numel() * out_dx.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        y = layer.forward(dev_in["x"], dev_in["topk_ids"], dev_in["topk_w"], wg, wu, wd)
+        out_y.copy_(y, non_blocking=True)
+        dx = layer.backward(dev_in["dy"], wg, wu, wd)[0]
+        out_dx.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = step_flops * world / (e2e_ms / args.steps * 1e-3) / 1e12
+    assert layer.device_error()[0] == B.MOE_OK
+
+    # ---------------- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    ms_k, n_k = per_kernel.get(ROOFLINE_KERNEL, (0.0, 0))
+    avg_ms = ms_k / n_k if n_k else float("nan")
+    kernel_flops = 6.0 * s.R * s.D * s.I          # G, U recompute + dA on the real rows
+    achieved = kernel_flops / (avg_ms * 1e-3) / 1e12 if n_k else None
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as fh:
+                traffic = json.load(fh).get(f"{s.name}:{ROOFLINE_KERNEL}")
+        except Exception:
+            traffic = None
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / args.steps}
+               for k, v in sorted(per_kernel.items())}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": s.name, "T": s.T, "D": s.D, "I": s.I, "E": s.E, "K": s.K,
+                   "align": 128, "router": s.router,
+                   "l2": "working set larger than L2 (expert weights alone 3*E*D*I*2 bytes)",
+                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        "fwd_frac_of_peak": fwd_tflops / peak_tf, "bwd_frac_of_peak": bwd_tflops / peak_tf,
+        "peak_bf16_tflops": peak_tf, "peak_source": peak_src,
+        "fwd_ms_median": statistics.median(fwd_ms), "bwd_ms_median": statistics.median(bwd_ms),
+        "step_ms_median": statistics.median(step_ms),
+        "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                     "peak_source": f"bf16_tflops_sustained ({peak_src})"},
+        "kernels": kernels,
+        "gpu_launches": int(launches1 - launches0),
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(s)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

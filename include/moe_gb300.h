@@ -69,7 +69,8 @@ size_t moe_capacity(int T, int K, int E, int align);
 /*
  * Bytes of scratch the layer needs: a 1 KB header (device error word), routing
  * chunk counters, the dW split schedule, the activation act [cap, I], the hidden
- * gradient [cap, 2I] and the routed output gradient [cap, D] (bf16).  One
+ * gradient [cap, 2I] (bf16 and fp16), the routed output gradient [cap, D] (bf16 and
+ * fp16) and an fp16 copy of x_perm [cap, D].  One
  * workspace may serve the forward and the backward of the same sizes, but not
  * two calls running concurrently.  Returns 0 for invalid arguments.
  */
@@ -134,14 +135,19 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
 
 /*
  * Expert MLP backward on the sorted rows ("LigerMoE design / Backward pass"):
- *   1. routed expert-output gradient  dy_perm[s] = bf16(w_perm[s] * dy[perm_src[s] / K]) (0 on padding)
- *   2. recompute G = x_perm W_gate[e], U = x_perm W_up[e]; dA = dy_perm W_down[e]^T;
- *      act = silu(G) U, dG = dA U silu'(G), dU = dA silu(G)   (bf16, in the workspace)
+ *   1. routed expert-output gradient: the rows dy[perm_src[s] / K] (zero on padding); the
+ *      router weight w_perm[s] is applied in fp32 inside step 2
+ *   2. recompute G = x_perm W_gate[e], U = x_perm W_up[e]; dA = w_perm[s] * dy_row W_down[e]^T;
+ *      dG = dA U silu'(G), dU = dA silu(G)  (bf16 for step 3, fp16 copies for step 4),
+ *      and w_perm[s] * silu(G) U (fp16, for step 4)
  *   3. input gradient  dx_perm[s] = bf16( dG[s] W_gate[e]^T + dU[s] W_up[e]^T )
- *   4. weight gradients (fp32), accumulated over all of the expert's rows; experts with
- *      more than 2048 rows are split and the parts are TMA reduce-added:
- *        dw_down[e] = act_e^T dy_perm_e,  dw_gate[e] = x_perm_e^T dG_e,  dw_up[e] = x_perm_e^T dU_e
- *      Experts with no rows get exactly zero.
+ *   4. weight gradients (fp32), summed over all of the expert's rows:
+ *        dw_down[e] = sum_s (w act)_s^T dy_row_s,  dw_gate[e] = x_perm_e^T dG_e,
+ *        dw_up[e] = x_perm_e^T dU_e
+ *      computed from fp16 operands (x and dy convert exactly; the intermediates keep 10
+ *      mantissa bits) with fp32 accumulation; experts with more than 2048 rows are split
+ *      over several tiles whose parts are TMA reduce-added.  Experts with no rows get
+ *      exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
  *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets from moe_route_permute, weights as in
  *   the forward -- all device.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
  *   dw_gate [E,D,I] fp32, dw_up [E,D,I] fp32, dw_down [E,I,D] fp32 (fully overwritten).

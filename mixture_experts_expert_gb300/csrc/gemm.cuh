@@ -18,7 +18,11 @@
 //           accumulators; epilogue writes act = silu(G) U, dG = dA U silu'(G), dU = dA silu(G)
 //   Dx      dx_perm[s]  = [dG dU][s] [W_g[e]; W_u[e]]^T                       (K = 2I)
 //   DwGU    [dW_g dW_u][e] = x_perm_e^T [dG dU]_e        (K = the expert's token rows)
-//   DwD     dW_d[e]        = act_e^T dy_perm_e
+//   DwD     dW_d[e]        = (w act)_e^T dy_perm_e
+// The weight-gradient GEMMs sum over up to thousands of token rows, so their operands
+// are fp16 copies (10-bit mantissa; x and dY convert exactly) rather than bf16: the
+// rounding of the intermediates (dG, dU, w*act) is what bounds dW's absolute error.
+// BwdAct applies the router weight to dA in fp32 (dy_perm holds the unscaled dY rows).
 // dW tiles cover at most kDwChunkRows token rows; an expert with more rows is split
 // across tiles whose fp32 results are TMA reduce-added into a zeroed dW.
 #pragma once
@@ -190,8 +194,9 @@ __device__ __forceinline__ void mma_issue(const GemmParams& p, GemmBarriers* bar
   // (a K-major | MN-major, b K-major | MN-major, N)
   constexpr bool kAmn = Tr::kIsDw;
   constexpr bool kBmn = (KIND != GemmKind::Dx);
-  constexpr uint32_t kIdesc = umma_idesc_bf16(128, 256, kAmn, kBmn);
-  constexpr uint32_t kIdescDA = umma_idesc_bf16(128, 128, false, false);  // BwdAct dA phase
+  // The weight-gradient GEMMs read fp16 operands (they touch no weights); the rest bf16.
+  constexpr uint32_t kIdesc = umma_idesc_f16kind(128, 256, kAmn, kBmn, Tr::kIsDw);
+  constexpr uint32_t kIdescDA = umma_idesc_f16kind(128, 128, false, false, false);
   const uint32_t a_lbo = kAmn ? 8192u : 16u;
   const uint32_t a_step = kAmn ? 2048u : 32u;
   const uint32_t b_lbo = kBmn ? 8192u : 16u;
@@ -255,7 +260,7 @@ __device__ __forceinline__ uint8_t* ring_next(uint8_t* base, int& ring, int lane
   return b;
 }
 
-// 32 rows x 32 bf16 (64-byte rows), 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r>>1)&3).
+// 32 rows x 32 16-bit values (64-byte rows), 64-byte swizzle: 16-byte chunk c of row r sits at c ^ ((r>>1)&3).
 __device__ __forceinline__ void stage_bf16_row(uint8_t* buf, int lane, const uint32_t (&pk)[16]) {
   uint8_t* rowp = buf + lane * 64;
   const int x = (lane >> 1) & 3;
@@ -368,6 +373,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
       }
     } else if constexpr (KIND == GemmKind::BwdAct) {
+      const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
       for (int c = 0; c < 4; ++c) {
         uint32_t g[32], u[32], da[32];
         tmem_ld32(tb + 32 * c, g);
@@ -376,7 +382,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         tmem_ld_wait(g);
         tmem_ld_after_wait(u);
         tmem_ld_after_wait(da);
-        uint32_t pa[16], pg[16], pu[16];
+        uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float r[2][3];
@@ -384,26 +390,35 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
           for (int h = 0; h < 2; ++h) {
             const float gv = __uint_as_float(g[2 * i + h]);
             const float uv = __uint_as_float(u[2 * i + h]);
-            const float dv = __uint_as_float(da[2 * i + h]);
+            const float dv = wr * __uint_as_float(da[2 * i + h]);
             const float sg = sigmoidf_fast(gv);
             const float si = gv * sg;
-            r[h][0] = si * uv;                                   // act
+            r[h][0] = wr * si * uv;                              // w * act (dW_down operand)
             r[h][1] = dv * uv * sg * (1.0f + gv * (1.0f - sg));  // dG
             r[h][2] = dv * si;                                   // dU
           }
-          pa[i] = pack_bf16x2(r[0][0], r[1][0]);
+          pa[i] = pack_f16x2(r[0][0], r[1][0]);
           pg[i] = pack_bf16x2(r[0][1], r[1][1]);
           pu[i] = pack_bf16x2(r[0][2], r[1][2]);
+          pg16[i] = pack_f16x2(r[0][1], r[1][1]);
+          pu16[i] = pack_f16x2(r[0][2], r[1][2]);
         }
+        const int col = ti.n0 + 32 * c;
         uint8_t* b0 = ring_next<4, 2048>(stg, ring, lane);
         stage_bf16_row(b0, lane, pa);
-        store_box(&p.mapO0, b0, ti.n0 + 32 * c, row, lane, false);
+        store_box(&p.mapO0, b0, col, row, lane, false);        // w*act, fp16
         uint8_t* b1 = ring_next<4, 2048>(stg, ring, lane);
         stage_bf16_row(b1, lane, pg);
-        store_box(&p.mapO1, b1, ti.n0 + 32 * c, row, lane, false);
+        store_box(&p.mapO1, b1, col, row, lane, false);        // dG, bf16
         uint8_t* b2 = ring_next<4, 2048>(stg, ring, lane);
         stage_bf16_row(b2, lane, pu);
-        store_box(&p.mapO1, b2, p.I + ti.n0 + 32 * c, row, lane, false);
+        store_box(&p.mapO1, b2, p.I + col, row, lane, false);  // dU, bf16
+        uint8_t* b3 = ring_next<4, 2048>(stg, ring, lane);
+        stage_bf16_row(b3, lane, pg16);
+        store_box(&p.mapO2, b3, col, row, lane, false);        // dG, fp16
+        uint8_t* b4 = ring_next<4, 2048>(stg, ring, lane);
+        stage_bf16_row(b4, lane, pu16);
+        store_box(&p.mapO2, b4, p.I + col, row, lane, false);  // dU, fp16
       }
     } else {  // DwGU, DwD: fp32 out, plain store or split-K reduce-add
       for (int c = 0; c < 8; ++c) {

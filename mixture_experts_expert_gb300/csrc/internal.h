@@ -26,7 +26,7 @@ enum KernelId : int {
   kKGemmGateUp,
   kKGemmDown,
   kKCombine,
-  kKDispatchDy,
+  kKBwdPrepRows,
   kKGemmBwdAct,
   kKGemmDx,
   kKDwPrep,
@@ -65,6 +65,7 @@ struct GemmParams {
   CUtensorMap mapO2;
   const int* offsets;      // [E+1] padded expert offsets (device)
   const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
+  const float* w_perm;     // [cap] router weight per sorted row (BwdAct)
   int* err;                // device error word
   int E, D, I;
   int n_tiles;             // N tiles per M tile
@@ -84,6 +85,14 @@ cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, 
 cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, const float* w_perm,
                                const int32_t* offsets, int E, int K, int D, int cap,
                                uint16_t* dst, int kernel_id, cudaStream_t s);
+
+// Backward operand preparation for every sorted row s < offsets[E]:
+//   dy_perm[s] = dy[perm_src[s] / K] (bf16, unscaled), dy16[s] = fp16 of the same row,
+//   x16[s] = fp16(x_perm[s]); zero rows on padding.
+cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x_perm,
+                                 const int32_t* perm_src, const int32_t* offsets, int E, int K,
+                                 int D, int cap, uint16_t* dy_perm, uint16_t* dy16,
+                                 uint16_t* x16, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
                            int T, int K, int D, uint16_t* out, cudaStream_t s);

@@ -15,7 +15,7 @@ namespace moe {
 // ------------------------------------------------------------------ launch bookkeeping
 static const char* const kKernelNames[kNumKernelIds] = {
     "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
-    "gemm_down",   "combine",    "dispatch_dy",   "gemm_bwd_act", "gemm_dx",
+    "gemm_down",   "combine",    "bwd_prep_rows", "gemm_bwd_act", "gemm_dx",
     "dw_prep",     "gemm_dw_gateup", "gemm_dw_down"};
 
 const char* kernel_name(int id) {
@@ -109,33 +109,40 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+enum class Elem { BF16, F16, F32 };
+
 // 2-D map over a row-major [outer, inner] tensor with a box of [box_outer, box_inner].
-static bool make_map(CUtensorMap* m, bool f32, const void* base, uint64_t inner, uint64_t outer,
+static bool make_map(CUtensorMap* m, Elem el, const void* base, uint64_t inner, uint64_t outer,
                      uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const bool f32 = el == Elem::F32;
   const uint64_t esize = f32 ? 4 : 2;
+  const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : (el == Elem::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * esize};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-            const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Operand load maps (128-byte swizzle, 64-element inner box) and store maps.
 static bool map_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows) {
-  return make_map(m, false, b, inner, outer, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  return make_map(m, Elem::BF16, b, inner, outer, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-static bool map_mnmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
-  return make_map(m, false, b, inner, outer, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+static bool map_mnmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer,
+                        Elem el = Elem::BF16) {
+  return make_map(m, el, b, inner, outer, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-static bool map_store_bf16(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
-  return make_map(m, false, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+static bool map_store_16(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer,
+                         Elem el = Elem::BF16) {
+  return make_map(m, el, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 static bool map_store_f32(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer) {
-  return make_map(m, true, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  return make_map(m, Elem::F32, b, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // ------------------------------------------------------------------ sizes
@@ -155,10 +162,11 @@ static size_t capacity_of(int T, int K, int E, int align) {
 static size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 
 struct WsLayout {
-  size_t chunk_counts, dw_prefix, act, dh, dyp, total;
+  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, total;
 };
 
-// header | routing chunk counters | dW split prefix | act | dH | dy_perm
+// header | routing chunk counters | dW split prefix | act | dH | dy_perm | dH fp16 |
+// dy_perm fp16 | x_perm fp16
 static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   WsLayout L;
   const size_t cap = capacity_of(T, K, E, align);
@@ -173,6 +181,12 @@ static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   L.dh = o;
   o = up1k(o + cap * static_cast<size_t>(I) * 4);
   L.dyp = o;
+  o = up1k(o + cap * static_cast<size_t>(D) * 2);
+  L.dh16 = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 4);
+  L.dyp16 = o;
+  o = up1k(o + cap * static_cast<size_t>(D) * 2);
+  L.xp16 = o;
   o = up1k(o + cap * static_cast<size_t>(D) * 2);
   L.total = o;
   return L;
@@ -292,7 +306,7 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   bool ok = map_kmajor(&p.mapA0, x_perm, D, cap, 128) &&
             map_mnmajor(&p.mapB0, w_gate, I, static_cast<uint64_t>(E) * D) &&
             map_mnmajor(&p.mapB1, w_up, I, static_cast<uint64_t>(E) * D) &&
-            map_store_bf16(&p.mapO0, act, I, cap);
+            map_store_16(&p.mapO0, act, I, cap);
   if (!ok) return MOE_ERR_CUDA;
   p.n_tiles = I / 128;
   cudaError_t e;
@@ -308,7 +322,7 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   q.E = E; q.D = D; q.I = I;
   ok = map_kmajor(&q.mapA0, act, I, cap, 128) &&
        map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I) &&
-       map_store_bf16(&q.mapO0, y_perm, D, cap);
+       map_store_16(&q.mapO0, y_perm, D, cap);
   if (!ok) return MOE_ERR_CUDA;
   q.n_tiles = D / 256;
   {
@@ -350,18 +364,25 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   const uint64_t ED = static_cast<uint64_t>(E) * D, EI = static_cast<uint64_t>(E) * I;
   cudaError_t e;
 
-  // 1. routed expert-output gradient
-  e = launch_gather_rows(dy, perm_src, w_perm, offsets, E, K, D, static_cast<int>(cap), dyp,
-                         kKDispatchDy, s);
+  void* dh16 = ws + L.dh16;
+  moe_bf16_t* dyp16 = reinterpret_cast<moe_bf16_t*>(ws + L.dyp16);
+  moe_bf16_t* xp16 = reinterpret_cast<moe_bf16_t*>(ws + L.xp16);
+
+  // 1. routed expert-output gradient rows (unscaled; the router weight is applied to dA in
+  //    fp32) and the fp16 operand copies of the weight-gradient GEMMs
+  e = launch_bwd_prep_rows(dy, x_perm, perm_src, offsets, E, K, D, static_cast<int>(cap), dyp,
+                           dyp16, xp16, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. recompute + dA + SwiGLU'
   GemmParams a{};
-  a.offsets = offsets; a.err = err; a.E = E; a.D = D; a.I = I;
+  a.offsets = offsets; a.w_perm = w_perm; a.err = err; a.E = E; a.D = D; a.I = I;
   bool ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) && map_kmajor(&a.mapA1, dyp, D, cap, 128) &&
             map_mnmajor(&a.mapB0, w_gate, I, ED) && map_mnmajor(&a.mapB1, w_up, I, ED) &&
-            map_kmajor(&a.mapB2, w_down, D, EI, 128) && map_store_bf16(&a.mapO0, act, I, cap) &&
-            map_store_bf16(&a.mapO1, dh, 2ull * I, cap);
+            map_kmajor(&a.mapB2, w_down, D, EI, 128) &&
+            map_store_16(&a.mapO0, act, I, cap, Elem::F16) &&
+            map_store_16(&a.mapO1, dh, 2ull * I, cap) &&
+            map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16);
   if (!ok) return MOE_ERR_CUDA;
   a.n_tiles = I / 128;
   {
@@ -374,7 +395,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   GemmParams x{};
   x.offsets = offsets; x.err = err; x.E = E; x.D = D; x.I = I;
   ok = map_kmajor(&x.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&x.mapB0, w_gate, I, ED, 256) &&
-       map_kmajor(&x.mapB1, w_up, I, ED, 256) && map_store_bf16(&x.mapO0, dx_perm, D, cap);
+       map_kmajor(&x.mapB1, w_up, I, ED, 256) && map_store_16(&x.mapO0, dx_perm, D, cap);
   if (!ok) return MOE_ERR_CUDA;
   x.n_tiles = D / 256;
   {
@@ -383,13 +404,14 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 4. weight gradients
+  // 4. weight gradients (fp16 operands, fp32 accumulate and output)
   e = launch_dw_prep(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int max_chunks = E + static_cast<int>(cap / kDwChunkRows) + 1;
   GemmParams g{};
   g.offsets = offsets; g.dw_prefix = dw_prefix; g.err = err; g.E = E; g.D = D; g.I = I;
-  ok = map_mnmajor(&g.mapA0, x_perm, D, cap) && map_mnmajor(&g.mapB0, dh, 2ull * I, cap) &&
+  ok = map_mnmajor(&g.mapA0, xp16, D, cap, Elem::F16) &&
+       map_mnmajor(&g.mapB0, dh16, 2ull * I, cap, Elem::F16) &&
        map_store_f32(&g.mapO0, dw_gate, I, ED) && map_store_f32(&g.mapO1, dw_up, I, ED);
   if (!ok) return MOE_ERR_CUDA;
   g.m_tiles = D / 128;
@@ -401,7 +423,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams d{};
   d.offsets = offsets; d.dw_prefix = dw_prefix; d.err = err; d.E = E; d.D = D; d.I = I;
-  ok = map_mnmajor(&d.mapA0, act, I, cap) && map_mnmajor(&d.mapB0, dyp, D, cap) &&
+  ok = map_mnmajor(&d.mapA0, act, I, cap, Elem::F16) &&
+       map_mnmajor(&d.mapB0, dyp16, D, cap, Elem::F16) &&
        map_store_f32(&d.mapO0, dw_down, D, EI);
   if (!ok) return MOE_ERR_CUDA;
   d.m_tiles = I / 128;

@@ -228,6 +228,67 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, con
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ backward row prep
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 q) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&q);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
+    w[i] = pack_f16x2(f.x, f.y);
+  }
+  return q;
+}
+
+// For every sorted row s < offsets[E]: dy_perm[s] = dy[perm_src[s]/K] (bf16 copy),
+// dy16[s] = the same row in fp16, x16[s] = fp16(x_perm[s]); zero rows on padding.
+__global__ void __launch_bounds__(256) k_bwd_prep_rows(
+    const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x_perm,
+    const int32_t* __restrict__ perm_src, const int32_t* __restrict__ offsets, int E, int K,
+    int D, uint16_t* __restrict__ dy_perm, uint16_t* __restrict__ dy16,
+    uint16_t* __restrict__ x16) {
+  const int rows = __ldg(offsets + E);
+  const int lane = threadIdx.x & 31;
+  const int nvec = D >> 3;
+  const int wpg = (gridDim.x * blockDim.x) >> 5;
+  for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < rows; s += wpg) {
+    const int j = __ldg(perm_src + s);
+    const size_t off = static_cast<size_t>(s) * D;
+    uint4* dp = reinterpret_cast<uint4*>(dy_perm + off);
+    uint4* d16 = reinterpret_cast<uint4*>(dy16 + off);
+    uint4* x16p = reinterpret_cast<uint4*>(x16 + off);
+    const uint4* xp = reinterpret_cast<const uint4*>(x_perm + off);
+    if (j < 0) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < nvec; v += 32) {
+        dp[v] = z;
+        d16[v] = z;
+        x16p[v] = z;
+      }
+      continue;
+    }
+    const uint4* sp = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(j / K) * D);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 q = __ldg(sp + v);
+      const uint4 xq = __ldg(xp + v);
+      dp[v] = q;
+      d16[v] = bf16x8_to_f16x8(q);
+      x16p[v] = bf16x8_to_f16x8(xq);
+    }
+  }
+}
+
+cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x_perm,
+                                 const int32_t* perm_src, const int32_t* offsets, int E, int K,
+                                 int D, int cap, uint16_t* dy_perm, uint16_t* dy16,
+                                 uint16_t* x16, cudaStream_t s) {
+  int blocks = (cap + 7) / 8;
+  if (blocks < 1) blocks = 1;
+  LaunchScope ls(kKBwdPrepRows, s);
+  k_bwd_prep_rows<<<blocks, 256, 0, s>>>(dy, x_perm, perm_src, offsets, E, K, D, dy_perm, dy16,
+                                         x16);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ combine
 // out[t] = sum_k w[t,k] * src[inv[t*K+k]] in fp32, k ascending, one warp per token.
 __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ src,
@@ -241,7 +302,10 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ sr
   const float my_w = lane < K ? (w ? __ldg(w + static_cast<size_t>(t) * K + lane) : 1.0f) : 0.f;
   const int nvec = D >> 3;
   uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * D);
-  for (int v = lane; v < nvec; v += 32) {
+  // warp-uniform trip count: every lane takes part in the shuffles of every step
+  for (int vb = 0; vb < nvec; vb += 32) {
+    const int v = vb + lane;
+    const bool act = v < nvec;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -253,8 +317,9 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ sr
         const int k = k0 + u;
         const int row = __shfl_sync(0xffffffffu, my_row, k & 31);
         wk[u] = __shfl_sync(0xffffffffu, my_w, k & 31);
-        q[u] = k < K ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D) + v)
-                     : make_uint4(0, 0, 0, 0);
+        q[u] = (act && k < K)
+                   ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D) + v)
+                   : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -268,8 +333,9 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ sr
         }
       }
     }
-    o[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    if (act)
+      o[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
   }
 }
 

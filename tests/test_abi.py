@@ -85,6 +85,6 @@ def test_workspace_grows_with_every_dimension(lib):
 
 def test_kernel_names_and_counters(lib):
     names = B.kernel_names()
-    assert "gemm_gateup_swiglu" in names and "gemm_dw_down" in names and "combine" in names
+    assert "gemm_gateup_swiglu" in names and "gemm_dw_down" in names and "combine" in names and "bwd_prep_rows" in names
     total, per = B.moe_launch_count()
     assert total == sum(per.values())

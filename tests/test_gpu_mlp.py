@@ -30,13 +30,13 @@ def _lib():
     B.lib()
 
 
-def random_layer(T, D, I, E, K, seed, ids=None, w_std=None):
+def random_layer(T, D, I, E, K, seed, ids=None, w_std=0.02):
+    """Inputs drawn like the workloads: x, dY ~ N(0,1), weights ~ N(0, 0.02)."""
     g = torch.Generator().manual_seed(seed)
-    w_std = w_std if w_std is not None else 1.0 / np.sqrt(D)
     x = torch.randn(T, D, generator=g).to(torch.bfloat16)
     wg = (torch.randn(E, D, I, generator=g) * w_std).to(torch.bfloat16)
     wu = (torch.randn(E, D, I, generator=g) * w_std).to(torch.bfloat16)
-    wd = (torch.randn(E, I, D, generator=g) * (1.0 / np.sqrt(I))).to(torch.bfloat16)
+    wd = (torch.randn(E, I, D, generator=g) * w_std).to(torch.bfloat16)
     dy = torch.randn(T, D, generator=g).to(torch.bfloat16)
     if ids is None:
         ids, w = synth.random_routing(T, K, E, seed=seed + 1)
@@ -121,8 +121,8 @@ def _sample_experts(counts, rng):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.SKEWED, synth.LLAMA4_SCOUT],
-                         ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.SKEWED, synth.SKEWED_STEEP,
+                                   synth.LLAMA4_SCOUT], ids=lambda s: s.name)
 def test_full_size_workloads_sampled(shape):
     s = shape
     inp_dev = synth.make_inputs(s, device=DEV)
