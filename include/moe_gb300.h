@@ -162,6 +162,32 @@ int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm, const int
                        void* workspace, void* stream);
 
 /*
+ * moe_route_permute without a workspace, for callers that cannot allocate device
+ * memory: code that only receives pointers to its tensors (a plugin or operator
+ * interface whose host framework owns every allocation), or an engine whose device
+ * memory is carved out once up front.  This entry point has no counterpart on the
+ * pages the library follows; it is an interface convenience.
+ *
+ * Arguments, outputs and results are exactly those of moe_route_permute (bit for bit)
+ * minus `workspace`.  The per-chunk expert counters live instead in one fixed 1 MiB
+ * array inside the library (every GPU that loads the library keeps it until the
+ * process exits), so E * ceil(T*K / 256) must not exceed 262080; larger sizes return
+ * MOE_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *
+ * The first call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.  All calls share the one
+ * array, so two calls whose kernels overlap on the GPU (different streams, or different
+ * host threads) race and corrupt each other's result; serialise them.  Expert ids
+ * outside [0, E) are skipped without being reported (moe_route_permute reports them).
+ */
+int moe_route_permute_noalloc(const int32_t* topk_ids, const float* topk_w,
+                              const moe_bf16_t* x, int T, int K, int E, int D, int align,
+                              int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                              int32_t* inv_perm, float* w_perm, moe_bf16_t* x_perm,
+                              void* stream);
+
+/*
  * Reads and clears the device error word of `workspace` (synchronises `stream`).
  * *code receives MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT; *detail the
  * raw device code (which role timed out).  For tests and debugging.

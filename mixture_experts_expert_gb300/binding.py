@@ -48,6 +48,8 @@ _SIGS = {
     "moe_expert_mlp_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _P, _P, _P, _P, _P, _P]),
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), _P]),
+    "moe_route_permute_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                       _P]),
     "moe_num_kernels": (_I, []),
     "moe_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_launch_count": (ctypes.c_longlong, [ctypes.POINTER(ctypes.c_longlong)]),
@@ -142,6 +144,19 @@ def moe_route_permute(topk_ids, topk_w, x, T, K, E, D, align, counts, offsets, p
         _ptr(w_perm, f32, "w_perm"), _ptr(x_perm, bf, "x_perm", x is None),
         _ptr(workspace, name="workspace"), _stream(stream))
     _check("moe_route_permute", st)
+
+
+def moe_route_permute_noalloc(topk_ids, topk_w, x, T, K, E, D, align, counts, offsets,
+                              perm_src, inv_perm, w_perm, x_perm, stream=None):
+    """moe_route_permute for callers that cannot allocate a workspace (see the header)."""
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    st = lib().moe_route_permute_noalloc(
+        _ptr(topk_ids, i32, "topk_ids", T == 0), _ptr(topk_w, f32, "topk_w", T == 0),
+        _ptr(x, bf, "x", True), T, K, E, D, align,
+        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"),
+        _ptr(perm_src, i32, "perm_src"), _ptr(inv_perm, i32, "inv_perm", T == 0),
+        _ptr(w_perm, f32, "w_perm"), _ptr(x_perm, bf, "x_perm", x is None), _stream(stream))
+    _check("moe_route_permute_noalloc", st)
 
 
 def moe_expert_mlp_fwd(x_perm, w_gate, w_up, w_down, offsets, T, K, E, D, I, align, y_perm,

@@ -402,3 +402,84 @@ cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float*
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------ routing without a workspace
+// moe_route_permute needs a caller-provided workspace for its per-chunk expert counters.
+// Some callers have no way to obtain device memory for it: code that only receives
+// pointers to its tensors (a plugin or operator ABI whose host framework owns every
+// allocation), or an engine whose device memory is carved out once up front and may not
+// grow afterwards.  moe_route_permute_noalloc serves them: its counters live in a
+// fixed array compiled into this library, so the caller passes only inputs and outputs.
+#include <mutex>
+
+namespace moe {
+namespace {
+
+// 1 MiB: the chunk counters need E * ceil(T*K / 256) ints, plus one error word.
+constexpr int kNoAllocScratchInts = 1 << 18;
+constexpr int kNoAllocErrWord = kNoAllocScratchInts - 64;   // last 256 bytes: the error word
+static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
+
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_scratch[64] = {};   // device address of g_route_scratch, per device
+
+// Host code cannot use g_route_scratch's name as a device pointer; look the address up once
+// per device (with that device current) and keep it.
+int32_t* noalloc_scratch_for_current_device(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_scratch[dev] == nullptr) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_noalloc_scratch[dev] = static_cast<int32_t*>(p);
+  }
+  return g_noalloc_scratch[dev];
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" __attribute__((visibility("default"))) int moe_route_permute_noalloc(
+    const int32_t* topk_ids, const float* topk_w, const uint16_t* x, int T, int K, int E, int D,
+    int align, int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
+    float* w_perm, uint16_t* x_perm, void* stream) {
+  using namespace moe;
+  // the same argument rules as moe_route_permute
+  if (T < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || align < 1) return -1;
+  const long long R = static_cast<long long>(T) * K;
+  const long long capl = R + static_cast<long long>(E) * (align - 1) + align;
+  if (R >= (1ll << 31) || capl >= (1ll << 31)) return -1;
+  if (!counts || !offsets || !perm_src || !w_perm) return -1;
+  if (T > 0 && (!topk_ids || !topk_w || !inv_perm)) return -1;
+  if (x && (!x_perm || D <= 0 || D % 8 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
+            (reinterpret_cast<uintptr_t>(x_perm) & 15)))
+    return -1;
+  // the counters must fit the fixed array
+  const long long need = static_cast<long long>(E) * route_num_chunks(static_cast<int>(R));
+  if (need > kNoAllocErrWord) return -2;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return -3;
+  if (major != 10 || minor != 3) return -2;
+  cudaError_t e = cudaSuccess;
+  int32_t* scratch = noalloc_scratch_for_current_device(&e);
+  if (!scratch) return -3;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the error word must start at zero
+  // (the chunk counters are fully rewritten by every call)
+  if (cudaMemsetAsync(scratch + kNoAllocErrWord, 0, sizeof(int32_t), s) != cudaSuccess) return -3;
+  const size_t cap = (static_cast<size_t>(R) + static_cast<size_t>(E) * (align - 1) + align - 1) /
+                     align * align;
+  e = launch_route(topk_ids, topk_w, x, T, K, E, D, align, static_cast<int>(cap), counts, offsets,
+                   perm_src, inv_perm, w_perm, x_perm, scratch, scratch + kNoAllocErrWord, s);
+  return e == cudaSuccess ? 0 : -3;
+}
