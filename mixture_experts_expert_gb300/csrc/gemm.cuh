@@ -14,8 +14,10 @@
 // Kinds (row-major everywhere; "perm" buffers are expert-sorted, padded to 128 rows):
 //   GateUp  act[s, i]   = silu(x_perm[s] W_g[e])_i * (x_perm[s] W_u[e])_i    N-tile: 128 gate + 128 up
 //   Down    y_perm[s]   = act[s] W_d[e]
-//   BwdAct  recompute G, U (K = D) and dA = dy_perm[s] W_d[e]^T (K = D) into three TMEM
-//           accumulators; epilogue writes act = silu(G) U, dG = dA U silu'(G), dU = dA silu(G)
+//   BwdAct  dA = dy_perm[s] W_d[e]^T (K = D) into one of two TMEM dA buffers, then the
+//           recompute G, U (K = D) into the single G|U buffer; epilogue writes w*act,
+//           dG = dA U silu'(G), dU = dA silu(G).  The next tile's dA phase overlaps this
+//           tile's epilogue; its G|U phase waits until the epilogue has read G and U.
 //   Dx      dx_perm[s]  = [dG dU][s] [W_g[e]; W_u[e]]^T                       (K = 2I)
 //   DwGU    [dW_g dW_u][e] = x_perm_e^T [dG dU]_e        (K = the expert's token rows)
 //   DwD     dW_d[e]        = (w act)_e^T dy_perm_e
@@ -47,6 +49,7 @@ struct __align__(8) GemmBarriers {
   uint64_t empty[kStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t tempty_gu;   // BwdAct: the single G|U accumulator is free again
   uint32_t tmem_addr;
   int abort;
 };
@@ -56,8 +59,9 @@ struct KindTraits {
   static constexpr bool kTokenRows = (KIND == GemmKind::GateUp || KIND == GemmKind::Down ||
                                       KIND == GemmKind::BwdAct || KIND == GemmKind::Dx);
   static constexpr bool kIsDw = !kTokenRows;
-  static constexpr int kNumAcc = (KIND == GemmKind::BwdAct) ? 1 : 2;
-  static constexpr int kAccCols = 256;
+  static constexpr int kNumAcc = 2;
+  // BwdAct: G|U live in columns [0, 256) (one buffer), dA in [256, 384) / [384, 512)
+  static constexpr int kAccCols = (KIND == GemmKind::BwdAct) ? 128 : 256;
   // output columns per tile along N
   static constexpr int kTileN = (KIND == GemmKind::GateUp || KIND == GemmKind::BwdAct) ? 128 : 256;
 };
@@ -69,6 +73,7 @@ struct TileInfo {
   int row0;   // dW: first token row of the K range
   int nkb;    // number of 64-deep K blocks
   int split;  // dW: the expert is split over several tiles (reduce-add)
+  int kb_half;  // dW of a split expert: K blocks per operand pass (hi, then lo)
 };
 
 // Largest e in [0, E) with arr[e] <= v (arr non-decreasing, arr[0] <= v < arr[E]).
@@ -95,6 +100,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
   TileInfo ti;
   ti.split = 0;
   ti.row0 = 0;
+  ti.kb_half = 0;
   if constexpr (KindTraits<KIND>::kTokenRows) {
     const int mt = t / p.n_tiles;
     const int nt = t - mt * p.n_tiles;
@@ -120,6 +126,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
     rows = rows < kDwChunkRows ? rows : kDwChunkRows;
     ti.nkb = rows > 0 ? rows / kBK : 0;
     ti.split = nch > 1;
+    ti.kb_half = ti.nkb;
+    if (ti.split) ti.nkb *= 2;   // compensated operands: the hi pass, then the lo pass
     const int mt = l / p.n_tiles;
     const int nt = l - mt * p.n_tiles;
     ti.m0 = mt * kBM;
@@ -143,9 +151,11 @@ __device__ __forceinline__ void produce(const GemmParams& p, GemmBarriers* bars,
       uint8_t* sB = sA + kStageBOffset;
       uint64_t* fb = &bars->full[stage];
       if constexpr (KIND == GemmKind::GateUp || KIND == GemmKind::BwdAct) {
+        // BwdAct runs its dA phase (dy rows x W_d^T) first, then the G|U recompute
         const int KB = p.D / kBK;
-        if (KIND == GemmKind::GateUp || kb < KB) {
-          const int k0 = kb * kBK;
+        const bool gu = KIND == GemmKind::GateUp || kb >= KB;
+        if (gu) {
+          const int k0 = (KIND == GemmKind::GateUp ? kb : kb - KB) * kBK;
           const int wy = ti.e * p.D + k0;
           mbar_arrive_expect_tx(fb, 48 * 1024);
           tma_load_2d(&p.mapA0, fb, sA, k0, ti.m0);
@@ -154,7 +164,7 @@ __device__ __forceinline__ void produce(const GemmParams& p, GemmBarriers* bars,
           tma_load_2d(&p.mapB1, fb, sB + 16384, ti.n0, wy);
           tma_load_2d(&p.mapB1, fb, sB + 24576, ti.n0 + 64, wy);
         } else {
-          const int k0 = (kb - KB) * kBK;
+          const int k0 = kb * kBK;
           mbar_arrive_expect_tx(fb, 32 * 1024);
           tma_load_2d(&p.mapA1, fb, sA, k0, ti.m0);
           tma_load_2d(&p.mapB2, fb, sB, k0, ti.e * p.I + ti.n0);
@@ -173,12 +183,17 @@ __device__ __forceinline__ void produce(const GemmParams& p, GemmBarriers* bars,
         if (k0 < p.I) tma_load_2d(&p.mapB0, fb, sB, k0, ti.e * p.D + ti.n0);
         else tma_load_2d(&p.mapB1, fb, sB, k0 - p.I, ti.e * p.D + ti.n0);
       } else {  // DwGU, DwD: both operands MN-major, K runs over token rows
-        const int s0 = ti.row0 + kb * kBK;
+        // a split expert runs its rows twice: with the fp16 values, then with their
+        // fp16 residuals (lo = v - fp16(v)) of the rounded operand, into one accumulator
+        const bool lo = ti.split && kb >= ti.kb_half;
+        const int s0 = ti.row0 + (lo ? kb - ti.kb_half : kb) * kBK;
+        const CUtensorMap* ma = (KIND == GemmKind::DwD && lo) ? &p.mapA1 : &p.mapA0;
+        const CUtensorMap* mb = (KIND == GemmKind::DwGU && lo) ? &p.mapB1 : &p.mapB0;
         mbar_arrive_expect_tx(fb, 48 * 1024);
-        tma_load_2d(&p.mapA0, fb, sA, ti.m0, s0);
-        tma_load_2d(&p.mapA0, fb, sA + 8192, ti.m0 + 64, s0);
+        tma_load_2d(ma, fb, sA, ti.m0, s0);
+        tma_load_2d(ma, fb, sA + 8192, ti.m0 + 64, s0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tma_load_2d(&p.mapB0, fb, sB + j * 8192, ti.n0 + 64 * j, s0);
+        for (int j = 0; j < 4; ++j) tma_load_2d(mb, fb, sB + j * 8192, ti.n0 + 64 * j, s0);
       }
       if (++stage == kStages) { stage = 0; phase ^= 1u; }
     }
@@ -206,6 +221,7 @@ __device__ __forceinline__ void mma_issue(const GemmParams& p, GemmBarriers* bar
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
+  uint32_t gu_phase = 0;
   const int ntiles = num_tiles<KIND>(p);
   const int KB = p.D / kBK;
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -213,18 +229,35 @@ __device__ __forceinline__ void mma_issue(const GemmParams& p, GemmBarriers* bar
     if (ti.nkb == 0) continue;
     if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort, p.err, kDevTimeoutMma)) return;
     tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Tr::kAccCols);
+    // BwdAct: dA of this tile goes to buffer acc, G|U to the shared columns [0, 256)
+    const uint32_t d_tmem = (KIND == GemmKind::BwdAct)
+                                ? tmem_base
+                                : tmem_base + static_cast<uint32_t>(acc * Tr::kAccCols);
+    const uint32_t d_da = tmem_base + 256u + static_cast<uint32_t>(acc * 128);
     for (int kb = 0; kb < ti.nkb; ++kb) {
+      if (KIND == GemmKind::BwdAct && kb == KB) {
+        // the previous tile's epilogue must have read G and U before they are overwritten
+        if (!mbar_wait(&bars->tempty_gu, gu_phase ^ 1u, abort, p.err, kDevTimeoutMma)) return;
+        gu_phase ^= 1u;
+        tc_fence_after();
+      }
       if (!mbar_wait(&bars->full[stage], phase, abort, p.err, kDevTimeoutMma)) return;
       tc_fence_after();
       const uint32_t sa = smem_u32(stages + stage * kStageBytes);
       const uint32_t sb = sa + kStageBOffset;
-      if (KIND == GemmKind::BwdAct && kb >= KB) {
+      if (KIND == GemmKind::BwdAct && kb < KB) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint64_t ad = umma_desc_sw128(sa + 32u * k, 16u, 1024u);
           const uint64_t bd = umma_desc_sw128(sb + 32u * k, 16u, 1024u);
-          umma_bf16(d_tmem + 256u, ad, bd, kIdescDA, (kb > KB || k > 0) ? 1u : 0u);
+          umma_bf16(d_da, ad, bd, kIdescDA, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+      } else if (KIND == GemmKind::BwdAct) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = umma_desc_sw128(sa + a_step * k, a_lbo, 1024u);
+          const uint64_t bd = umma_desc_sw128(sb + b_step * k, b_lbo, 1024u);
+          umma_bf16(d_tmem, ad, bd, kIdesc, (kb > KB || k > 0) ? 1u : 0u);
         }
       } else {
 #pragma unroll
@@ -238,12 +271,8 @@ __device__ __forceinline__ void mma_issue(const GemmParams& p, GemmBarriers* bar
       if (++stage == kStages) { stage = 0; phase ^= 1u; }
     }
     umma_commit(&bars->tfull[acc]);
-    if (Tr::kNumAcc == 2) {
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    } else {
-      acc_phase ^= 1u;
-    }
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
   }
 }
 
@@ -293,6 +322,12 @@ __device__ __forceinline__ void store_box(const CUtensorMap* map, const uint8_t*
   __syncwarp();
 }
 
+// fp16 residuals (v0 - fp16(v0), v1 - fp16(v1)) given the packed fp16 pair.
+__device__ __forceinline__ uint32_t f16x2_residual(uint32_t packed, float v0, float v1) {
+  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&packed));
+  return pack_f16x2(v0 - hf.x, v1 - hf.y);
+}
+
 __device__ __forceinline__ void pack_row(const float (&v)[32], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -337,8 +372,11 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
     __syncwarp();
     if (!ok) return;
     tc_fence_after();
-    const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                        static_cast<uint32_t>(acc * Tr::kAccCols);
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    const uint32_t tb = (KIND == GemmKind::BwdAct)
+                            ? lane_base
+                            : lane_base + static_cast<uint32_t>(acc * Tr::kAccCols);
+    const uint32_t tda = lane_base + 256u + static_cast<uint32_t>(acc * 128);
 
     if constexpr (KIND == GemmKind::GateUp) {
       for (int c = 0; c < 4; ++c) {
@@ -374,15 +412,18 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
       }
     } else if constexpr (KIND == GemmKind::BwdAct) {
       const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
+      // rows of an expert whose dW is split over several tiles also get the fp16 residuals
+      const bool want_lo =
+          (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
       for (int c = 0; c < 4; ++c) {
         uint32_t g[32], u[32], da[32];
         tmem_ld32(tb + 32 * c, g);
         tmem_ld32(tb + 128 + 32 * c, u);
-        tmem_ld32(tb + 256 + 32 * c, da);
+        tmem_ld32(tda + 32 * c, da);
         tmem_ld_wait(g);
         tmem_ld_after_wait(u);
         tmem_ld_after_wait(da);
-        uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16];
+        uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16], la[16], lg[16], lu[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           float r[2][3];
@@ -402,6 +443,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
           pu[i] = pack_bf16x2(r[0][2], r[1][2]);
           pg16[i] = pack_f16x2(r[0][1], r[1][1]);
           pu16[i] = pack_f16x2(r[0][2], r[1][2]);
+          la[i] = f16x2_residual(pa[i], r[0][0], r[1][0]);
+          lg[i] = f16x2_residual(pg16[i], r[0][1], r[1][1]);
+          lu[i] = f16x2_residual(pu16[i], r[0][2], r[1][2]);
         }
         const int col = ti.n0 + 32 * c;
         uint8_t* b0 = ring_next<4, 2048>(stg, ring, lane);
@@ -419,6 +463,17 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         uint8_t* b4 = ring_next<4, 2048>(stg, ring, lane);
         stage_bf16_row(b4, lane, pu16);
         store_box(&p.mapO2, b4, p.I + col, row, lane, false);  // dU, fp16
+        if (want_lo) {
+          uint8_t* c0 = ring_next<4, 2048>(stg, ring, lane);
+          stage_bf16_row(c0, lane, la);
+          store_box(&p.mapO3, c0, col, row, lane, false);        // w*act residual
+          uint8_t* c1 = ring_next<4, 2048>(stg, ring, lane);
+          stage_bf16_row(c1, lane, lg);
+          store_box(&p.mapO4, c1, col, row, lane, false);        // dG residual
+          uint8_t* c2 = ring_next<4, 2048>(stg, ring, lane);
+          stage_bf16_row(c2, lane, lu);
+          store_box(&p.mapO4, c2, p.I + col, row, lane, false);  // dU residual
+        }
       }
     } else {  // DwGU, DwD: fp32 out, plain store or split-K reduce-add
       for (int c = 0; c < 8; ++c) {
@@ -441,13 +496,12 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->tempty[acc]);
-    if (Tr::kNumAcc == 2) {
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    } else {
-      acc_phase ^= 1u;
+    if (lane == 0) {
+      mbar_arrive(&bars->tempty[acc]);
+      if (KIND == GemmKind::BwdAct) mbar_arrive(&bars->tempty_gu);
     }
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
   }
 }
 
@@ -474,6 +528,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_grouped_gemm(const __grid_c
       mbar_init(&bars->tfull[i], 1);
       mbar_init(&bars->tempty[i], kEpiWarps);
     }
+    mbar_init(&bars->tempty_gu, kEpiWarps);
     bars->abort = 0;
     fence_mbarrier_init();
   }

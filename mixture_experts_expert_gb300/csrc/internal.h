@@ -63,6 +63,8 @@ struct GemmParams {
   CUtensorMap mapO0;
   CUtensorMap mapO1;
   CUtensorMap mapO2;
+  CUtensorMap mapO3;
+  CUtensorMap mapO4;
   const int* offsets;      // [E+1] padded expert offsets (device)
   const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
   const float* w_perm;     // [cap] router weight per sorted row (BwdAct)

@@ -162,11 +162,12 @@ static size_t capacity_of(int T, int K, int E, int align) {
 static size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 
 struct WsLayout {
-  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, total;
+  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, total;
 };
 
 // header | routing chunk counters | dW split prefix | act | dH | dy_perm | dH fp16 |
-// dy_perm fp16 | x_perm fp16
+// dy_perm fp16 | x_perm fp16 | w*act fp16 residual | dH fp16 residual (the residuals
+// are written only for experts whose weight gradient is split over several tiles)
 static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   WsLayout L;
   const size_t cap = capacity_of(T, K, E, align);
@@ -188,6 +189,10 @@ static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   o = up1k(o + cap * static_cast<size_t>(D) * 2);
   L.xp16 = o;
   o = up1k(o + cap * static_cast<size_t>(D) * 2);
+  L.act_lo = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 2);
+  L.dh16_lo = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 4);
   L.total = o;
   return L;
 }
@@ -367,6 +372,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   void* dh16 = ws + L.dh16;
   moe_bf16_t* dyp16 = reinterpret_cast<moe_bf16_t*>(ws + L.dyp16);
   moe_bf16_t* xp16 = reinterpret_cast<moe_bf16_t*>(ws + L.xp16);
+  void* act_lo = ws + L.act_lo;
+  void* dh16_lo = ws + L.dh16_lo;
 
   // 1. routed expert-output gradient rows (unscaled; the router weight is applied to dA in
   //    fp32) and the fp16 operand copies of the weight-gradient GEMMs
@@ -382,7 +389,9 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
             map_kmajor(&a.mapB2, w_down, D, EI, 128) &&
             map_store_16(&a.mapO0, act, I, cap, Elem::F16) &&
             map_store_16(&a.mapO1, dh, 2ull * I, cap) &&
-            map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16);
+            map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16) &&
+            map_store_16(&a.mapO3, act_lo, I, cap, Elem::F16) &&
+            map_store_16(&a.mapO4, dh16_lo, 2ull * I, cap, Elem::F16);
   if (!ok) return MOE_ERR_CUDA;
   a.n_tiles = I / 128;
   {
@@ -412,6 +421,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   g.offsets = offsets; g.dw_prefix = dw_prefix; g.err = err; g.E = E; g.D = D; g.I = I;
   ok = map_mnmajor(&g.mapA0, xp16, D, cap, Elem::F16) &&
        map_mnmajor(&g.mapB0, dh16, 2ull * I, cap, Elem::F16) &&
+       map_mnmajor(&g.mapB1, dh16_lo, 2ull * I, cap, Elem::F16) &&
        map_store_f32(&g.mapO0, dw_gate, I, ED) && map_store_f32(&g.mapO1, dw_up, I, ED);
   if (!ok) return MOE_ERR_CUDA;
   g.m_tiles = D / 128;
@@ -424,6 +434,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   GemmParams d{};
   d.offsets = offsets; d.dw_prefix = dw_prefix; d.err = err; d.E = E; d.D = D; d.I = I;
   ok = map_mnmajor(&d.mapA0, act, I, cap, Elem::F16) &&
+       map_mnmajor(&d.mapA1, act_lo, I, cap, Elem::F16) &&
        map_mnmajor(&d.mapB0, dyp16, D, cap, Elem::F16) &&
        map_store_f32(&d.mapO0, dw_down, D, EI);
   if (!ok) return MOE_ERR_CUDA;
