@@ -28,7 +28,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE expert-MLP TFLOP/s fwd & bwd on 1 GB300 (% of BF16 dense peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-ROOFLINE_KERNEL = "gemm_bwd_act"
+# Algorithmic FLOPs of each tensor-core kernel per launch, in units of R*D*I (R = T*K
+# routed rows; padding rows excluded).
+GEMM_FLOPS_RDI = {"gemm_gateup_swiglu": 4, "gemm_down": 2, "gemm_dA": 2, "gemm_bwd_gateup": 4,
+                  "gemm_dx": 4, "gemm_dw_gateup": 4, "gemm_dw_down": 2}
 
 
 def parse():
@@ -325,24 +328,30 @@ def main():
     e2e_value = step_flops * world / (e2e_ms / args.steps * 1e-3) / 1e12
     assert layer.device_error()[0] == B.MOE_OK
 
-    # ---------------- roofline of the dominant kernel
+    # ---------------- roofline of the dominant kernel (largest share of the step)
     peaks, peak_src = load_peaks()
-    ms_k, n_k = per_kernel.get(ROOFLINE_KERNEL, (0.0, 0))
-    avg_ms = ms_k / n_k if n_k else float("nan")
-    kernel_flops = 6.0 * s.R * s.D * s.I          # G, U recompute + dA on the real rows
-    achieved = kernel_flops / (avg_ms * 1e-3) / 1e12 if n_k else None
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    rdi = s.R * s.D * s.I
+    kernels = {}
+    for k, (ms_k, n_k) in sorted(per_kernel.items()):
+        ent = {"ms_per_launch": ms_k / n_k, "launches_per_step": n_k / args.steps}
+        if k in GEMM_FLOPS_RDI:
+            tf = GEMM_FLOPS_RDI[k] * rdi / (ms_k / n_k * 1e-3) / 1e12
+            ent["tflops"] = tf
+            ent["frac_of_sustained_peak"] = tf / peak
+        kernels[k] = ent
+    gemms = {k: v for k, v in per_kernel.items() if k in GEMM_FLOPS_RDI}
+    dom = max(gemms, key=lambda k: gemms[k][0]) if gemms else None
+    achieved = kernels[dom]["tflops"] if dom else None
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
+    if dom and os.path.exists(prof):
         try:
             with open(prof) as fh:
-                traffic = json.load(fh).get(f"{s.name}:{ROOFLINE_KERNEL}")
+                traffic = json.load(fh).get(f"{s.name}:{dom}")
         except Exception:
             traffic = None
-    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches_per_step": v[1] / args.steps}
-               for k, v in sorted(per_kernel.items())}
 
     if rank != 0:
         if world > 1:
@@ -363,7 +372,7 @@ def main():
         "peak_bf16_tflops": peak_tf, "peak_source": peak_src,
         "fwd_ms_median": statistics.median(fwd_ms), "bwd_ms_median": statistics.median(bwd_ms),
         "step_ms_median": statistics.median(step_ms),
-        "roofline": {"kernel": ROOFLINE_KERNEL, "bound": "tensor", "achieved": achieved,
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                      "peak_source": f"bf16_tflops_sustained ({peak_src})"},

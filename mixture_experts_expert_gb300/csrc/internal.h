@@ -27,7 +27,8 @@ enum KernelId : int {
   kKGemmDown,
   kKCombine,
   kKBwdPrepRows,
-  kKGemmBwdAct,
+  kKGemmDA,
+  kKGemmBwdGU,
   kKGemmDx,
   kKDwPrep,
   kKGemmDwGU,
@@ -47,7 +48,7 @@ struct LaunchScope {
 };
 
 // Grouped-GEMM variants (one tcgen05 kernel template, one instantiation each).
-enum class GemmKind : int { GateUp = 0, Down = 1, BwdAct = 2, Dx = 3, DwGU = 4, DwD = 5 };
+enum class GemmKind : int { GateUp = 0, Down = 1, DA = 2, BwdGU = 3, Dx = 4, DwGU = 5, DwD = 6 };
 
 // Tile sizes shared by host and device.
 constexpr int kBM = 128;        // token rows (or feature rows for dW) per tile
@@ -67,11 +68,13 @@ struct GemmParams {
   CUtensorMap mapO4;
   const int* offsets;      // [E+1] padded expert offsets (device)
   const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
-  const float* w_perm;     // [cap] router weight per sorted row (BwdAct)
+  const float* w_perm;     // [cap] router weight per sorted row (DA, BwdGU)
+  const float* dA;         // [cap, I] router-weighted dA, fp32 (BwdGU reads it)
   int* err;                // device error word
   int E, D, I;
   int n_tiles;             // N tiles per M tile
   int m_tiles;             // M tiles per expert (dW kinds)
+  int tile_n;              // DA: output columns per tile (256, or 128 when I % 256 != 0)
 };
 
 // Launch one grouped GEMM; `max_tiles` bounds the device-side tile count.

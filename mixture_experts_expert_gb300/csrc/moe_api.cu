@@ -15,8 +15,8 @@ namespace moe {
 // ------------------------------------------------------------------ launch bookkeeping
 static const char* const kKernelNames[kNumKernelIds] = {
     "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
-    "gemm_down",   "combine",    "bwd_prep_rows", "gemm_bwd_act", "gemm_dx",
-    "dw_prep",     "gemm_dw_gateup", "gemm_dw_down"};
+    "gemm_down",   "combine",    "bwd_prep_rows", "gemm_dA",    "gemm_bwd_gateup",
+    "gemm_dx",     "dw_prep",    "gemm_dw_gateup", "gemm_dw_down"};
 
 const char* kernel_name(int id) {
   return (id >= 0 && id < kNumKernelIds) ? kKernelNames[id] : nullptr;
@@ -162,12 +162,13 @@ static size_t capacity_of(int T, int K, int E, int align) {
 static size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 
 struct WsLayout {
-  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, total;
+  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, da, total;
 };
 
 // header | routing chunk counters | dW split prefix | act | dH | dy_perm | dH fp16 |
 // dy_perm fp16 | x_perm fp16 | w*act fp16 residual | dH fp16 residual (the residuals
-// are written only for experts whose weight gradient is split over several tiles)
+// are written only for experts whose weight gradient is split over several tiles) |
+// router-weighted dA fp32
 static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   WsLayout L;
   const size_t cap = capacity_of(T, K, E, align);
@@ -192,6 +193,8 @@ static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   L.act_lo = o;
   o = up1k(o + cap * static_cast<size_t>(I) * 2);
   L.dh16_lo = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 4);
+  L.da = o;
   o = up1k(o + cap * static_cast<size_t>(I) * 4);
   L.total = o;
   return L;
@@ -381,22 +384,35 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
                            dyp16, xp16, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 2. recompute + dA + SwiGLU'
+  // 2. dA = w * dy_perm W_d^T (fp32), then the gate/up recompute with the SwiGLU' epilogue
+  float* dA = reinterpret_cast<float*>(ws + L.da);
+  GemmParams da{};
+  da.offsets = offsets; da.w_perm = w_perm; da.err = err; da.E = E; da.D = D; da.I = I;
+  da.tile_n = (I % 256 == 0) ? 256 : 128;
+  bool ok = map_kmajor(&da.mapA0, dyp, D, cap, 128) &&
+            map_kmajor(&da.mapB0, w_down, D, EI, static_cast<uint32_t>(da.tile_n)) &&
+            map_store_f32(&da.mapO0, dA, I, cap);
+  if (!ok) return MOE_ERR_CUDA;
+  da.n_tiles = I / da.tile_n;
+  {
+    LaunchScope ls(kKGemmDA, s);
+    e = launch_gemm_kind<GemmKind::DA>(da, m_tiles_max * da.n_tiles, f->num_sms, s);
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams a{};
-  a.offsets = offsets; a.w_perm = w_perm; a.err = err; a.E = E; a.D = D; a.I = I;
-  bool ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) && map_kmajor(&a.mapA1, dyp, D, cap, 128) &&
-            map_mnmajor(&a.mapB0, w_gate, I, ED) && map_mnmajor(&a.mapB1, w_up, I, ED) &&
-            map_kmajor(&a.mapB2, w_down, D, EI, 128) &&
-            map_store_16(&a.mapO0, act, I, cap, Elem::F16) &&
-            map_store_16(&a.mapO1, dh, 2ull * I, cap) &&
-            map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16) &&
-            map_store_16(&a.mapO3, act_lo, I, cap, Elem::F16) &&
-            map_store_16(&a.mapO4, dh16_lo, 2ull * I, cap, Elem::F16);
+  a.offsets = offsets; a.w_perm = w_perm; a.dA = dA; a.err = err; a.E = E; a.D = D; a.I = I;
+  ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) &&
+       map_mnmajor(&a.mapB0, w_gate, I, ED) && map_mnmajor(&a.mapB1, w_up, I, ED) &&
+       map_store_16(&a.mapO0, act, I, cap, Elem::F16) &&
+       map_store_16(&a.mapO1, dh, 2ull * I, cap) &&
+       map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16) &&
+       map_store_16(&a.mapO3, act_lo, I, cap, Elem::F16) &&
+       map_store_16(&a.mapO4, dh16_lo, 2ull * I, cap, Elem::F16);
   if (!ok) return MOE_ERR_CUDA;
   a.n_tiles = I / 128;
   {
-    LaunchScope ls(kKGemmBwdAct, s);
-    e = launch_gemm_kind<GemmKind::BwdAct>(a, m_tiles_max * a.n_tiles, f->num_sms, s);
+    LaunchScope ls(kKGemmBwdGU, s);
+    e = launch_gemm_kind<GemmKind::BwdGU>(a, m_tiles_max * a.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
