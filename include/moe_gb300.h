@@ -196,6 +196,17 @@ int moe_get_device_error(void* workspace, int* code, int* detail, void* stream);
 
 /* ---- diagnostics ---------------------------------------------------------- */
 
+/*
+ * Test hook for the failure path.  Makes the next grouped-GEMM launch of the calling
+ * host thread (the gate/up GEMM of the next moe_expert_mlp_fwd) issue no loads.  Its
+ * MMA and epilogue warps then wait on barriers nothing completes; each wait gives up
+ * after about one second, the kernel lets in-flight work drain, frees its tensor memory
+ * and returns, and the workspace error word reads MOE_ERR_DEVICE_TIMEOUT.  Nothing
+ * faults, traps or hangs, and the context stays usable.  The outputs of that call are
+ * undefined.
+ */
+int moe_debug_drop_next_loads(void);
+
 /* Number of distinct kernels; kernel ids are 0 .. moe_num_kernels()-1. */
 int moe_num_kernels(void);
 

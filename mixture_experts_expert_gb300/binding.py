@@ -50,6 +50,7 @@ _SIGS = {
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), _P]),
     "moe_route_permute_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                        _P]),
+    "moe_debug_drop_next_loads": (_I, []),
     "moe_num_kernels": (_I, []),
     "moe_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_launch_count": (ctypes.c_longlong, [ctypes.POINTER(ctypes.c_longlong)]),
@@ -197,6 +198,11 @@ def moe_get_device_error(workspace, stream=None):
         _ptr(workspace, name="workspace"), ctypes.byref(code), ctypes.byref(detail),
         _stream(stream)))
     return code.value, detail.value
+
+
+def moe_debug_drop_next_loads():
+    """Test hook: the next gate/up GEMM launch skips its loads so its waits time out."""
+    _check("moe_debug_drop_next_loads", lib().moe_debug_drop_next_loads())
 
 
 def kernel_names() -> list[str]:

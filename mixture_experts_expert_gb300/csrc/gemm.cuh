@@ -196,6 +196,7 @@ __device__ __forceinline__ void produce(const GemmParams& p, GemmBarriers* bars,
   uint32_t phase = 0;
   const int ntiles = num_tiles<KIND>(p);
   const uint32_t bytes = kblock_bytes<KIND>(p);
+  if (p.drop_loads) return;   // test hook: nothing arrives, the consumers' waits expire
   for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const TileInfo ti = decode_tile<KIND>(p, t);
     for (int kb = 0; kb < ti.nkb; ++kb) {

@@ -75,6 +75,7 @@ struct GemmParams {
   int n_tiles;             // N tiles per M tile
   int m_tiles;             // M tiles per expert (dW kinds)
   int tile_n;              // DA: output columns per tile (256, or 128 when I % 256 != 0)
+  int drop_loads;          // test hook: the producer issues nothing, so the waits expire
 };
 
 // Launch one grouped GEMM; `max_tiles` bounds the device-side tile count.

@@ -216,6 +216,15 @@ static bool gemm_shape_ok(int D, int I, int align) {
 
 static int to_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Test hook (moe_debug_drop_next_loads): the next grouped-GEMM launch of this host thread
+// issues no loads, so its bounded waits run out and report a timeout.
+static thread_local bool t_drop_next_loads = false;
+static int take_drop_flag() {
+  const bool d = t_drop_next_loads;
+  t_drop_next_loads = false;
+  return d ? 1 : 0;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -317,6 +326,7 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
             map_store_16(&p.mapO0, act, I, cap);
   if (!ok) return MOE_ERR_CUDA;
   p.n_tiles = I / 128;
+  p.drop_loads = take_drop_flag();
   cudaError_t e;
   {
     LaunchScope ls(kKGemmGateUp, s);
@@ -478,6 +488,11 @@ MOE_EXPORT int moe_get_device_error(void* workspace, int* code, int* detail, voi
     if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   }
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_debug_drop_next_loads(void) {
+  t_drop_next_loads = true;
   return MOE_OK;
 }
 

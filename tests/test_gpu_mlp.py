@@ -121,7 +121,8 @@ def _sample_experts(counts, rng):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.SKEWED, synth.SKEWED_STEEP,
+@pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.sweep_shape(1024),
+                                   synth.sweep_shape(2048), synth.SKEWED, synth.SKEWED_STEEP,
                                    synth.LLAMA4_SCOUT], ids=lambda s: s.name)
 def test_full_size_workloads_sampled(shape):
     s = shape
