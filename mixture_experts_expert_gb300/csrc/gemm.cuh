@@ -147,10 +147,9 @@ __device__ __forceinline__ void issue_kblock(const GemmParams& p, const TileInfo
     const int k0 = kb * kBK;
     const int wy = ti.e * p.D + k0;
     tma_load_2d(&p.mapA0, fb, sA, k0, ti.m0);
-    tma_load_2d(&p.mapB0, fb, sB, ti.n0, wy);
-    tma_load_2d(&p.mapB0, fb, sB + 8192, ti.n0 + 64, wy);
-    tma_load_2d(&p.mapB1, fb, sB + 16384, ti.n0, wy);
-    tma_load_2d(&p.mapB1, fb, sB + 24576, ti.n0 + 64, wy);
+    // MN-major weight operands load as 3-D boxes: (64 columns) x (64 K rows) x (atoms)
+    tma_load_3d(&p.mapB0, fb, sB, 0, wy, ti.n0 / 64);           // 2 gate atoms
+    tma_load_3d(&p.mapB1, fb, sB + 16384, 0, wy, ti.n0 / 64);   // 2 up atoms
   } else if constexpr (KIND == GemmKind::DA) {
     // B = W_d[e] rows (features) as N x K, K-major: one box of tile_n rows
     const int k0 = kb * kBK;
@@ -160,8 +159,7 @@ __device__ __forceinline__ void issue_kblock(const GemmParams& p, const TileInfo
     const int k0 = kb * kBK;
     const int wy = ti.e * p.I + k0;
     tma_load_2d(&p.mapA0, fb, sA, k0, ti.m0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(&p.mapB0, fb, sB + j * 8192, ti.n0 + 64 * j, wy);
+    tma_load_3d(&p.mapB0, fb, sB, 0, wy, ti.n0 / 64);           // 4 atoms
   } else if constexpr (KIND == GemmKind::Dx) {
     const int k0 = kb * kBK;
     tma_load_2d(&p.mapA0, fb, sA, k0, ti.m0);
@@ -174,10 +172,8 @@ __device__ __forceinline__ void issue_kblock(const GemmParams& p, const TileInfo
     const int s0 = ti.row0 + (lo ? kb - ti.kb_half : kb) * kBK;
     const CUtensorMap* ma = (KIND == GemmKind::DwD && lo) ? &p.mapA1 : &p.mapA0;
     const CUtensorMap* mb = (KIND == GemmKind::DwGU && lo) ? &p.mapB1 : &p.mapB0;
-    tma_load_2d(ma, fb, sA, ti.m0, s0);
-    tma_load_2d(ma, fb, sA + 8192, ti.m0 + 64, s0);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(mb, fb, sB + j * 8192, ti.n0 + 64 * j, s0);
+    tma_load_3d(ma, fb, sA, 0, s0, ti.m0 / 64);   // 2 atoms
+    tma_load_3d(mb, fb, sB, 0, s0, ti.n0 / 64);   // 4 atoms
   }
 }
 

@@ -133,9 +133,22 @@ static bool make_map(CUtensorMap* m, Elem el, const void* base, uint64_t inner, 
 static bool map_kmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer, uint32_t rows) {
   return make_map(m, Elem::BF16, b, inner, outer, 64, rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
+// MN-major operand map over a row-major [outer, inner] tensor viewed in 3-D as
+// (64 columns, rows, inner / 64 column atoms), with a box of `atoms` 64x64 atoms: one TMA
+// load fills the atoms at 8 KB strides, the layout the MN-major descriptors expect.
 static bool map_mnmajor(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer,
-                        Elem el = Elem::BF16) {
-  return make_map(m, el, b, inner, outer, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+                        uint32_t atoms, Elem el = Elem::BF16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || inner % 64 != 0) return false;
+  const CUtensorMapDataType dt = el == Elem::F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {64, outer, inner / 64};
+  cuuint64_t strides[2] = {inner * 2, 128};
+  cuuint32_t box[3] = {64, 64, atoms};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(b), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 static bool map_store_16(CUtensorMap* m, const void* b, uint64_t inner, uint64_t outer,
                          Elem el = Elem::BF16) {
@@ -321,8 +334,8 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   p.E = E; p.D = D; p.I = I;
   // gate/up + SwiGLU
   bool ok = map_kmajor(&p.mapA0, x_perm, D, cap, 128) &&
-            map_mnmajor(&p.mapB0, w_gate, I, static_cast<uint64_t>(E) * D) &&
-            map_mnmajor(&p.mapB1, w_up, I, static_cast<uint64_t>(E) * D) &&
+            map_mnmajor(&p.mapB0, w_gate, I, static_cast<uint64_t>(E) * D, 2) &&
+            map_mnmajor(&p.mapB1, w_up, I, static_cast<uint64_t>(E) * D, 2) &&
             map_store_16(&p.mapO0, act, I, cap);
   if (!ok) return MOE_ERR_CUDA;
   p.n_tiles = I / 128;
@@ -339,7 +352,7 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   q.err = p.err;
   q.E = E; q.D = D; q.I = I;
   ok = map_kmajor(&q.mapA0, act, I, cap, 128) &&
-       map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I) &&
+       map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I, 4) &&
        map_store_16(&q.mapO0, y_perm, D, cap);
   if (!ok) return MOE_ERR_CUDA;
   q.n_tiles = D / 256;
@@ -412,7 +425,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   GemmParams a{};
   a.offsets = offsets; a.w_perm = w_perm; a.dA = dA; a.err = err; a.E = E; a.D = D; a.I = I;
   ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) &&
-       map_mnmajor(&a.mapB0, w_gate, I, ED) && map_mnmajor(&a.mapB1, w_up, I, ED) &&
+       map_mnmajor(&a.mapB0, w_gate, I, ED, 2) && map_mnmajor(&a.mapB1, w_up, I, ED, 2) &&
        map_store_16(&a.mapO0, act, I, cap, Elem::F16) &&
        map_store_16(&a.mapO1, dh, 2ull * I, cap) &&
        map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16) &&
@@ -445,9 +458,9 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   const int max_chunks = E + static_cast<int>(cap / kDwChunkRows) + 1;
   GemmParams g{};
   g.offsets = offsets; g.dw_prefix = dw_prefix; g.err = err; g.E = E; g.D = D; g.I = I;
-  ok = map_mnmajor(&g.mapA0, xp16, D, cap, Elem::F16) &&
-       map_mnmajor(&g.mapB0, dh16, 2ull * I, cap, Elem::F16) &&
-       map_mnmajor(&g.mapB1, dh16_lo, 2ull * I, cap, Elem::F16) &&
+  ok = map_mnmajor(&g.mapA0, xp16, D, cap, 2, Elem::F16) &&
+       map_mnmajor(&g.mapB0, dh16, 2ull * I, cap, 4, Elem::F16) &&
+       map_mnmajor(&g.mapB1, dh16_lo, 2ull * I, cap, 4, Elem::F16) &&
        map_store_f32(&g.mapO0, dw_gate, I, ED) && map_store_f32(&g.mapO1, dw_up, I, ED);
   if (!ok) return MOE_ERR_CUDA;
   g.m_tiles = D / 128;
@@ -459,9 +472,9 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams d{};
   d.offsets = offsets; d.dw_prefix = dw_prefix; d.err = err; d.E = E; d.D = D; d.I = I;
-  ok = map_mnmajor(&d.mapA0, act, I, cap, Elem::F16) &&
-       map_mnmajor(&d.mapA1, act_lo, I, cap, Elem::F16) &&
-       map_mnmajor(&d.mapB0, dyp16, D, cap, Elem::F16) &&
+  ok = map_mnmajor(&d.mapA0, act, I, cap, 2, Elem::F16) &&
+       map_mnmajor(&d.mapA1, act_lo, I, cap, 2, Elem::F16) &&
+       map_mnmajor(&d.mapB0, dyp16, D, cap, 4, Elem::F16) &&
        map_store_f32(&d.mapO0, dw_down, D, EI);
   if (!ok) return MOE_ERR_CUDA;
   d.m_tiles = I / 128;
