@@ -49,46 +49,59 @@ __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
   return v;
 }
 
-// One 1024-thread block: per expert, exclusive prefix over chunks (in place, giving each
-// chunk's first rank inside the expert); the expert counts; the padded offsets.
-__global__ void __launch_bounds__(1024) k_route_scan(int E, int nchunks, int align,
-                                                     int32_t* __restrict__ chunk_counts,
-                                                     int32_t* __restrict__ counts,
-                                                     int32_t* __restrict__ offsets) {
-  __shared__ int s_cnt[1024];
-  __shared__ int s_warp[32];
+// One warp per expert: exclusive prefix over its chunk counts (in place, giving each
+// chunk's first rank inside the expert) and the expert's total count.
+__global__ void __launch_bounds__(kRouteWarps * 32) k_route_scan(int E, int nchunks,
+                                                               int32_t* __restrict__ chunk_counts,
+                                                               int32_t* __restrict__ counts) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += 32) {
-    int32_t* row = chunk_counts + static_cast<size_t>(e) * nchunks;
-    int running = 0;
-    for (int cb = 0; cb < nchunks; cb += 32) {
-      const int c = cb + lane;
-      const int v = c < nchunks ? row[c] : 0;
-      const int incl = warp_incl_scan(v, lane);
-      if (c < nchunks) row[c] = running + incl - v;
-      running += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_cnt[e] = running;
+  const int e = blockIdx.x * kRouteWarps + warp;
+  if (e >= E) return;
+  int32_t* row = chunk_counts + static_cast<size_t>(e) * nchunks;
+  int running = 0;
+  for (int cb = 0; cb < nchunks; cb += 32) {
+    const int c = cb + lane;
+    const int v = c < nchunks ? row[c] : 0;
+    const int incl = warp_incl_scan(v, lane);
+    if (c < nchunks) row[c] = running + incl - v;
+    running += __shfl_sync(0xffffffffu, incl, 31);
   }
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int cnt = e < E ? s_cnt[e] : 0;
-  const int pad = (cnt + align - 1) / align * align;
-  const int incl = warp_incl_scan(pad, lane);
+  if (lane == 0) counts[e] = running;
+}
+
+// Exclusive scan of the padded expert counts into s_off[0..E] (one block; every thread
+// takes part).  Each block of the scatter kernel computes it for itself; block 0 also
+// publishes it as `offsets`.
+__device__ __forceinline__ void block_padded_offsets(const int32_t* __restrict__ counts, int E,
+                                                     int align, int* s_off, int* s_warp) {
+  const int nthr = blockDim.x;
+  const int per = (E + nthr - 1) / nthr;   // consecutive experts per thread
+  const int e0 = threadIdx.x * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) local += (__ldg(counts + e) + align - 1) / align * align;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int incl = warp_incl_scan(local, lane);
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int v = s_warp[lane];
-    const int wi = warp_incl_scan(v, lane);
-    s_warp[lane] = wi - v;
+    const int nw = nthr >> 5;
+    const int v = lane < nw ? s_warp[lane] : 0;
+    s_warp[lane] = warp_incl_scan(v, lane) - v;
   }
   __syncthreads();
-  const int excl = s_warp[warp] + incl - pad;
-  if (e < E) {
-    counts[e] = cnt;
-    offsets[e] = excl;
+  int run = s_warp[warp] + incl - local;
+  for (int i = 0; i < per; ++i) {
+    const int e = e0 + i;
+    if (e < E) {
+      s_off[e] = run;
+      run += (__ldg(counts + e) + align - 1) / align * align;
+    }
   }
-  if (e == E - 1) offsets[E] = excl + pad;
+  if (threadIdx.x == nthr - 1) s_off[E] = run;
+  __syncthreads();
 }
 
 // Stable scatter: each warp walks its chunk in slot order; equal experts inside a
@@ -96,16 +109,21 @@ __global__ void __launch_bounds__(1024) k_route_scan(int E, int nchunks, int ali
 // order across steps.  Slot j lands on row offsets[e] + (rank of j among e's slots).
 __global__ void __launch_bounds__(kRouteWarps * 32) k_route_scatter(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int R, int E, int nchunks,
-    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
-    int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
-    float* __restrict__ w_perm) {
+    int align, const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+    int32_t* __restrict__ inv_perm, float* __restrict__ w_perm) {
   extern __shared__ int sh_run[];
+  __shared__ int s_off[1025];
+  __shared__ int s_warp[32];
+  block_padded_offsets(counts, E, align, s_off, s_warp);
+  if (blockIdx.x == 0)
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kRouteWarps + warp;
   if (c >= nchunks) return;
   int* run = sh_run + warp * E;
   for (int e = lane; e < E; e += 32)
-    run[e] = __ldg(offsets + e) + chunk_base[static_cast<size_t>(e) * nchunks + c];
+    run[e] = s_off[e] + chunk_base[static_cast<size_t>(e) * nchunks + c];
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
   for (int it = 0; it < kChunk / 32; ++it) {
@@ -151,13 +169,16 @@ cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, 
   if (e != cudaSuccess) return e;
   {
     LaunchScope ls(kKRouteScan, s);
-    k_route_scan<<<1, 1024, 0, s>>>(E, nchunks, align, chunk_counts, counts, offsets);
+    k_route_scan<<<(E + kRouteWarps - 1) / kRouteWarps, kRouteWarps * 32, 0, s>>>(
+        E, nchunks, chunk_counts, counts);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (nchunks > 0) {
+  {
+    // (with no routed slots the scatter still runs one block, to publish the offsets)
     LaunchScope ls(kKRouteScatter, s);
-    k_route_scatter<<<blocks, kRouteWarps * 32, sh, s>>>(ids, w, R, E, nchunks, chunk_counts,
-                                                         offsets, perm_src, inv_perm, w_perm);
+    k_route_scatter<<<blocks, kRouteWarps * 32, sh, s>>>(ids, w, R, E, nchunks, align,
+                                                         chunk_counts, counts, offsets,
+                                                         perm_src, inv_perm, w_perm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (x != nullptr) {
@@ -302,40 +323,54 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ sr
   const float my_w = lane < K ? (w ? __ldg(w + static_cast<size_t>(t) * K + lane) : 1.0f) : 0.f;
   const int nvec = D >> 3;
   uint4* o = reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * D);
-  // warp-uniform trip count: every lane takes part in the shuffles of every step
-  for (int vb = 0; vb < nvec; vb += 32) {
-    const int v = vb + lane;
-    const bool act = v < nvec;
-    float acc[8];
+  // warp-uniform trip count: every lane takes part in the shuffles of every step; two
+  // vector columns per step keep 2 x 8 row loads in flight per lane
+  for (int vb = 0; vb < nvec; vb += 64) {
+    int vv[2];
+    bool act[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int h = 0; h < 2; ++h) {
+      vv[h] = vb + 32 * h + lane;
+      act[h] = vv[h] < nvec;
+    }
+    float acc[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[h][i] = 0.f;
     for (int k0 = 0; k0 < K; k0 += 8) {
-      uint4 q[8];
+      uint4 q[2][8];
       float wk[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u;
         const int row = __shfl_sync(0xffffffffu, my_row, k & 31);
         wk[u] = __shfl_sync(0xffffffffu, my_w, k & 31);
-        q[u] = (act && k < K)
-                   ? __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D) + v)
-                   : make_uint4(0, 0, 0, 0);
+        const uint4* rp = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          q[h][u] = (act[h] && k < K) ? __ldg(rp + vv[h]) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         if (k0 + u >= K) break;
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(&q[u]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[i]));
-          acc[2 * i] = fmaf(wk[u], f.x, acc[2 * i]);
-          acc[2 * i + 1] = fmaf(wk[u], f.y, acc[2 * i + 1]);
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t* qw = reinterpret_cast<const uint32_t*>(&q[h][u]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[i]));
+            acc[h][2 * i] = fmaf(wk[u], f.x, acc[h][2 * i]);
+            acc[h][2 * i + 1] = fmaf(wk[u], f.y, acc[h][2 * i + 1]);
+          }
         }
       }
     }
-    if (act)
-      o[v] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (act[h])
+        o[vv[h]] = make_uint4(pack_bf16x2(acc[h][0], acc[h][1]), pack_bf16x2(acc[h][2], acc[h][3]),
+                              pack_bf16x2(acc[h][4], acc[h][5]), pack_bf16x2(acc[h][6], acc[h][7]));
   }
 }
 
