@@ -222,6 +222,7 @@ def main():
     from mixture_experts_expert_gb300 import build as Bld
     from mixture_experts_expert_gb300 import synth
     from mixture_experts_expert_gb300.layer import MoEExpertMLP
+    from mixture_experts_expert_gb300.replicas import job_throughput, max_over_ranks
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -281,14 +282,10 @@ def main():
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     fwd_ms = [a.elapsed_time(b) for a, b in zip(starts, mids)]
     bwd_ms = [a.elapsed_time(b) for a, b in zip(mids, ends)]
-    total_ms = starts[0].elapsed_time(ends[-1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), dev)
     ms_per_step = total_ms / args.steps
     step_flops = s.fwd_flops() + s.bwd_flops()
-    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(step_flops, world, ms_per_step * 1e-3) / 1e12
     fwd_tflops = s.fwd_flops() / (statistics.median(fwd_ms) * 1e-3) / 1e12
     bwd_tflops = s.bwd_flops() / (statistics.median(bwd_ms) * 1e-3) / 1e12
 
@@ -320,12 +317,8 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = step_flops * world / (e2e_ms / args.steps * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_value = job_throughput(step_flops, world, e2e_ms / args.steps * 1e-3) / 1e12
     assert layer.device_error()[0] == B.MOE_OK
 
     # ---------------- roofline of the dominant kernel (largest share of the step)
