@@ -290,36 +290,71 @@ def main():
     bwd_tflops = s.bwd_flops() / (statistics.median(bwd_ms) * 1e-3) / 1e12
 
     # ---------------- end to end through host buffers (pinned), same step
-    host = {k: inp[k].cpu().pin_memory() for k in ("x", "topk_ids", "topk_w", "dy")}
-    out_y = torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory()
-    out_dx = torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory()
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    # Every step copies its inputs (x, ids, w, dY) in from pinned host memory and its
+    # results (Y, dX) out.  The copies run on a second stream and are double-buffered:
+    # step i+2's inputs are copied in and step i's results copied out while step i+1
+    # computes (results are first staged in device buffers so the next step may reuse the
+    # layer's own output tensors).
+    keys = ("x", "topk_ids", "topk_w", "dy")
+    host = {k: inp[k].cpu().pin_memory() for k in keys}
+    out_y = [torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    out_dx = [torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
+    stage_y = [torch.empty(s.T, s.D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    stage_dx = [torch.empty(s.T, s.D, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_y.numel() * out_y.element_size() + out_dx.numel() * out_dx.element_size()
+    d2h = out_y[0].numel() * out_y[0].element_size() + out_dx[0].numel() * out_dx[0].element_size()
+    copy = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d_done, staged, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-    def e2e_step():
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        y = layer.forward(dev_in["x"], dev_in["topk_ids"], dev_in["topk_w"], wg, wu, wd)
-        out_y.copy_(y, non_blocking=True)
-        dx = layer.backward(dev_in["dy"], wg, wu, wd)[0]
-        out_dx.copy_(dx, non_blocking=True)
+    def prefetch(b):
+        with torch.cuda.stream(copy):
+            for k in keys:
+                dev_in[b][k].copy_(host[k], non_blocking=True)
+            h2d_done[b].record(copy)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_step(i, n):
+        b = i % 2
+        stream.wait_event(h2d_done[b])
+        d = dev_in[b]
+        y = layer.forward(d["x"], d["topk_ids"], d["topk_w"], wg, wu, wd)
+        dx = layer.backward(d["dy"], wg, wu, wd)[0]
+        stream.wait_event(d2h_done[b])          # staging slot b has been copied out
+        stage_y[b].copy_(y)
+        stage_dx[b].copy_(dx)
+        staged[b].record(stream)
+        with torch.cuda.stream(copy):
+            copy.wait_event(staged[b])
+            out_y[b].copy_(stage_y[b], non_blocking=True)
+            out_dx[b].copy_(stage_dx[b], non_blocking=True)
+            d2h_done[b].record(copy)
+        if i + 2 < n:
+            prefetch(b)                          # inputs of step i + 2 (slot b is free)
+
+    def e2e_run(n):
+        copy.wait_stream(stream)
+        prefetch(0)
+        if n > 1:
+            prefetch(1)
+        for i in range(n):
+            e2e_step(i, n)
+        stream.wait_stream(copy)                 # the last results have reached the host
+
+    e2e_run(3)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = job_throughput(step_flops, world, e2e_ms / args.steps * 1e-3) / 1e12
     assert layer.device_error()[0] == B.MOE_OK
+    assert torch.equal(out_y[(args.steps - 1) % 2].to(dev), layer.y)
 
     # ---------------- roofline of the dominant kernel (largest share of the step)
     peaks, peak_src = load_peaks()
