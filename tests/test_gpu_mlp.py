@@ -97,6 +97,8 @@ def test_tiny_layer():
     (40, 256, 128, 16, 2, 1),     # most experts empty
     (1, 256, 128, 4, 1, 2),       # a single token
     (300, 768, 256, 3, 3, 3),     # D = 3 x 256, I = 2 x 128
+    (200, 256, 128, 1, 1, 4),     # a single expert
+    (512, 256, 128, 256, 8, 5),   # many experts with a handful of rows each (mostly padding)
 ])
 def test_small_layers(T, D, I, E, K, seed):
     check_full(random_layer(T, D, I, E, K, seed), T, D, I, E, K)
