@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef uint16_t moe_bf16_t;
 
@@ -113,13 +113,18 @@ int moe_route_permute(const int32_t* topk_ids, const float* topk_w, const moe_bf
  *   y_perm[s] = bf16( act[s] W_down[e] )                                  (fp32 accumulate)
  *   x_perm [cap,D] bf16, w_gate [E,D,I] bf16, w_up [E,D,I] bf16, w_down [E,I,D] bf16,
  *   offsets [E+1] int32 (from moe_route_permute with the same align) -- all device.
+ *   counts [E] int32 (device) or NULL: the real rows of each expert (moe_route_permute's
+ *   counts).  Rows of expert e at and past offsets[e] + counts[e] are padding; with counts
+ *   the GEMMs skip most of the padding of an expert's last row tile.  With NULL every row
+ *   below offsets[e+1] is computed (padding rows of x_perm are zero, so they give zero).
  *   y_perm [cap,D] bf16 (device): rows < offsets[E] written; padding rows come out zero.
  * act is kept in the workspace.  Needs D % 256 == 0, I % 128 == 0, align % 128 == 0.
  */
 int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_gate,
                        const moe_bf16_t* w_up, const moe_bf16_t* w_down,
-                       const int32_t* offsets, int T, int K, int E, int D, int I, int align,
-                       moe_bf16_t* y_perm, void* workspace, void* stream);
+                       const int32_t* offsets, const int32_t* counts, int T, int K, int E,
+                       int D, int I, int align, moe_bf16_t* y_perm, void* workspace,
+                       void* stream);
 
 /*
  * Token combine ("LigerMoE design": the forward's final local combine applies the
@@ -148,14 +153,14 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *      mantissa bits) with fp32 accumulation; experts with more than 2048 rows are split
  *      over several tiles whose parts are TMA reduce-added.  Experts with no rows get
  *      exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
- *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets from moe_route_permute, weights as in
- *   the forward -- all device.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
+ *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets/counts (counts may be NULL) from
+ *   moe_route_permute, weights as in the forward -- all device.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
  *   dw_gate [E,D,I] fp32, dw_up [E,D,I] fp32, dw_down [E,I,D] fp32 (fully overwritten).
  * Reduce dx_perm to tokens with moe_combine(dx_perm, inv_perm, NULL, ...).
  * Needs D % 256 == 0, I % 128 == 0, align % 128 == 0.
  */
 int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm, const int32_t* perm_src,
-                       const float* w_perm, const int32_t* offsets,
+                       const float* w_perm, const int32_t* offsets, const int32_t* counts,
                        const moe_bf16_t* w_gate, const moe_bf16_t* w_up,
                        const moe_bf16_t* w_down, int T, int K, int E, int D, int I, int align,
                        moe_bf16_t* dx_perm, float* dw_gate, float* dw_up, float* dw_down,

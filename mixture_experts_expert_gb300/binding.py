@@ -43,9 +43,9 @@ _SIGS = {
     "moe_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "moe_workspace_init": (_I, [_P, _P]),
     "moe_route_permute": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "moe_expert_mlp_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_expert_mlp_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
-    "moe_expert_mlp_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+    "moe_expert_mlp_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _P, _P, _P, _P, _P, _P]),
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), _P]),
     "moe_route_permute_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
@@ -160,12 +160,13 @@ def moe_route_permute_noalloc(topk_ids, topk_w, x, T, K, E, D, align, counts, of
     _check("moe_route_permute_noalloc", st)
 
 
-def moe_expert_mlp_fwd(x_perm, w_gate, w_up, w_down, offsets, T, K, E, D, I, align, y_perm,
-                       workspace, stream=None):
+def moe_expert_mlp_fwd(x_perm, w_gate, w_up, w_down, offsets, counts, T, K, E, D, I, align,
+                       y_perm, workspace, stream=None):
     bf = torch.bfloat16
     st = lib().moe_expert_mlp_fwd(
         _ptr(x_perm, bf, "x_perm"), _ptr(w_gate, bf, "w_gate"), _ptr(w_up, bf, "w_up"),
-        _ptr(w_down, bf, "w_down"), _ptr(offsets, torch.int32, "offsets"), T, K, E, D, I, align,
+        _ptr(w_down, bf, "w_down"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(counts, torch.int32, "counts", True), T, K, E, D, I, align,
         _ptr(y_perm, bf, "y_perm"), _ptr(workspace, name="workspace"), _stream(stream))
     _check("moe_expert_mlp_fwd", st)
 
@@ -179,12 +180,14 @@ def moe_combine(src_perm, inv_perm, topk_w, T, K, D, out, stream=None):
     _check("moe_combine", st)
 
 
-def moe_expert_mlp_bwd(dy, x_perm, perm_src, w_perm, offsets, w_gate, w_up, w_down, T, K, E, D,
-                       I, align, dx_perm, dw_gate, dw_up, dw_down, workspace, stream=None):
+def moe_expert_mlp_bwd(dy, x_perm, perm_src, w_perm, offsets, counts, w_gate, w_up, w_down, T,
+                       K, E, D, I, align, dx_perm, dw_gate, dw_up, dw_down, workspace,
+                       stream=None):
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     st = lib().moe_expert_mlp_bwd(
         _ptr(dy, bf, "dy", T == 0), _ptr(x_perm, bf, "x_perm"), _ptr(perm_src, i32, "perm_src"),
-        _ptr(w_perm, f32, "w_perm"), _ptr(offsets, i32, "offsets"), _ptr(w_gate, bf, "w_gate"),
+        _ptr(w_perm, f32, "w_perm"), _ptr(offsets, i32, "offsets"),
+        _ptr(counts, i32, "counts", True), _ptr(w_gate, bf, "w_gate"),
         _ptr(w_up, bf, "w_up"), _ptr(w_down, bf, "w_down"), T, K, E, D, I, align,
         _ptr(dx_perm, bf, "dx_perm"), _ptr(dw_gate, f32, "dw_gate"), _ptr(dw_up, f32, "dw_up"),
         _ptr(dw_down, f32, "dw_down"), _ptr(workspace, name="workspace"), _stream(stream))

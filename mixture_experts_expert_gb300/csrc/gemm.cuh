@@ -1,15 +1,24 @@
 // Persistent, warp-specialised grouped GEMM for the MoE expert MLP on sm_103a.
 //
 // One CTA per SM, 192 threads:
-//   warp 0      TMA producer (lane 0 issues cp.async.bulk.tensor into a ring of 48 KB stages)
-//   warp 1      TMEM owner + MMA issuer (lane 0 issues tcgen05.mma, M = 128, fp32 accumulators
-//               in two 256-column TMEM buffers, so one tile's epilogue overlaps the next
+//   warp 0      TMA producer (lane 0 issues cp.async.bulk.tensor into a ring of stages)
+//   warp 1      TMEM owner + MMA issuer (lane 0 issues tcgen05.mma, fp32 accumulators in
+//               two 256-column TMEM buffers, so one tile's epilogue overlaps the next
 //               tile's MMAs)
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lanes
 //               32*(w%4)..+31), fused elementwise math, tile stores or reduce-adds through a
 //               swizzled shared-memory ring and TMA.
 //
-// Tiles are scheduled statically (tile = blockIdx.x + i*gridDim.x) over a tile space
+// Token-row kinds run on CTA pairs (clusters of two): one M = 256 tcgen05.mma issued by the
+// even CTA covers two 128-row tiles of one expert, each CTA loading its own 128 rows of A
+// and half of the N columns of B.  A 64-deep K block then costs 32 KB of shared memory per
+// SM instead of 48 KB, so six stages fit where four did: the main loop is bound by load
+// latency, and the deeper ring hides more of it.  The pair's tile space enumerates, per
+// expert, ceil(m_tiles / 2) row pairs; when an expert has an odd number of row tiles the
+// odd CTA's half of its last pair is a ghost (loaded and multiplied, never stored).
+// The weight-gradient kinds (K = token rows, M = feature rows) run one CTA per tile, M = 128.
+//
+// Tiles are scheduled statically (tile = cta (or pair) index + i * count) over a tile space
 // whose size is read on the device from the expert offsets, so the launch is
 // independent of the routing (no host sync; valid inside a captured CUDA graph).
 //
@@ -36,9 +45,8 @@
 
 namespace moe {
 
-constexpr int kStageBytes = 48 * 1024;      // A: 128x64 16-bit (16 KB) + B: up to 256x64 (32 KB)
-constexpr int kStageBOffset = 16 * 1024;
-constexpr int kMaxStages = 4;
+constexpr int kStageBOffset = 16 * 1024;    // B follows A (128 x 64 16-bit = 16 KB) in a stage
+constexpr int kMaxStages = 6;
 constexpr int kEpiWarps = 4;
 constexpr int kGemmThreads = 192;
 constexpr int kTmemCols = 512;
@@ -48,6 +56,8 @@ struct __align__(8) GemmBarriers {
   uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t xfull[2];    // swapped gate/up tails: up warp -> gate warp exchange, per warp pair
+  uint64_t xempty[2];
   uint32_t tmem_addr;
   int abort;
 };
@@ -56,14 +66,24 @@ template <GemmKind KIND>
 struct KindTraits {
   static constexpr bool kIsDw = (KIND == GemmKind::DwGU || KIND == GemmKind::DwD);
   static constexpr bool kTokenRows = !kIsDw;
-  // Every kind is load-latency bound: four 48 KB stages in flight (three measured
-  // slower even for the write-heavy weight-gradient GEMMs, given a deeper store ring).
-  static constexpr int kStages = 4;
-  static constexpr int kEpiBytes = 8 * 1024;                          // staging per epilogue warp
+  static constexpr bool kPair = kTokenRows;   // M = 256 over a CTA pair
+  // weights stored N-contiguous (MN-major as the B operand / as the swapped A operand)
+  static constexpr bool kWeightsMN =
+      (KIND == GemmKind::GateUp || KIND == GemmKind::BwdGU || KIND == GemmKind::Down);
+  // Stage = A (128 x 64) + this CTA's B: half of N on a pair (<= 128 x 64), else up to 256 x 64.
+  static constexpr int kStageBytes = kPair ? 32 * 1024 : 48 * 1024;
+  // Every kind is load-latency bound, so stages take what the epilogue staging leaves
+  // (for the single-CTA kinds three stages measured slower than four even for the
+  // write-heavy weight-gradient GEMMs, given a deeper store ring).
+  static constexpr int kStages = !kPair ? 4 : (KIND == GemmKind::DA ? 5 : 6);
+  static constexpr int kEpiBytes =                                   // staging per epilogue warp
+      !kPair ? 8 * 1024 : (KIND == GemmKind::DA ? 12 * 1024 : 6 * 1024);
   static constexpr int kRing16 = kEpiBytes / 2048;                   // 2 KB 16-bit boxes
   static constexpr int kRing32 = kEpiBytes / 4096;                   // 4 KB fp32 boxes
-  static constexpr int kSmemBytes =
-      1024 /*barriers*/ + kStages * kStageBytes + kEpiWarps * kEpiBytes + 1024 /*align*/;
+  // pair kinds: per-expert prefix of row pairs, [0, E]
+  static constexpr int kPrefixBytes = kPair ? ((kMaxExperts + 1) * 4 + 127) / 128 * 128 : 0;
+  static constexpr int kSmemBytes = 1024 /*barriers*/ + kStages * kStageBytes +
+                                    kEpiWarps * kEpiBytes + kPrefixBytes + 1024 /*align*/;
   // output columns per tile along N (DA: p.tile_n at run time)
   static constexpr int kTileN = (KIND == GemmKind::GateUp || KIND == GemmKind::BwdGU) ? 128 : 256;
 };
@@ -76,6 +96,9 @@ struct TileInfo {
   int nkb;      // number of 64-deep K blocks
   int split;    // dW: the expert is split over several tiles (reduce-add)
   int kb_half;  // dW of a split expert: K blocks per operand pass (values, then residuals)
+  int ghost;    // pair kinds: this CTA's 128 rows lie past the expert's last row tile
+  int swap;     // pair kinds: the expert's odd last row tile, computed transposed
+  int tail_n;   // swap: token rows computed (a multiple of 32); the rest are padding
 };
 
 // Largest e in [0, E) with arr[e] <= v (arr non-decreasing, arr[0] <= v < arr[E]).
@@ -88,27 +111,112 @@ __device__ __forceinline__ int find_segment(const int* __restrict__ arr, int E, 
   return lo;
 }
 
+// The same search over a prefix held in shared memory.
+__device__ __forceinline__ int find_segment_smem(const int* arr, int E, int v) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (arr[mid] <= v) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Pair kinds: pfx[e] = number of 256-row pairs of experts before e (pfx[E] = all pairs),
+// an expert of m row tiles owning ceil(m / 2).  Computed by every CTA into shared memory
+// (all threads take part; the caller synchronises before use).
+__device__ __forceinline__ void build_pair_prefix(const GemmParams& p, int* pfx) {
+  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
+    const int mt = (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e)) / kBM;
+    pfx[e + 1] = (mt + 1) >> 1;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (p.E + 31) / 32;          // each lane scans a contiguous run of experts
+    const int b = lane * per;
+    const int end = b + per < p.E ? b + per : p.E;
+    int sum = 0;
+    for (int e = b; e < end; ++e) sum += pfx[e + 1];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int e = b; e < end; ++e) {
+      run += pfx[e + 1];
+      pfx[e + 1] = run;
+    }
+    if (lane == 0) pfx[0] = 0;
+  }
+}
+
 template <GemmKind KIND>
-__device__ __forceinline__ int num_tiles(const GemmParams& p) {
-  if constexpr (KindTraits<KIND>::kTokenRows) {
+__device__ __forceinline__ int num_tiles(const GemmParams& p, const int* pfx) {
+  if constexpr (KindTraits<KIND>::kPair) {
+    return pfx[p.E] * p.n_tiles;
+  } else if constexpr (KindTraits<KIND>::kTokenRows) {
     return (__ldg(p.offsets + p.E) / kBM) * p.n_tiles;
   } else {
     return __ldg(p.dw_prefix + p.E) * p.m_tiles * p.n_tiles;
   }
 }
 
+// First tile and stride of this CTA's static schedule (pairs step together).
 template <GemmKind KIND>
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+__device__ __forceinline__ int first_tile() {
+  if constexpr (KindTraits<KIND>::kPair) return static_cast<int>(cluster_id_x());
+  return blockIdx.x;
+}
+template <GemmKind KIND>
+__device__ __forceinline__ int tile_stride() {
+  if constexpr (KindTraits<KIND>::kPair) return static_cast<int>(num_clusters_x());
+  return gridDim.x;
+}
+
+template <GemmKind KIND>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, const int* pfx,
+                                                int rank) {
   TileInfo ti;
   ti.split = 0;
   ti.row0 = 0;
   ti.kb_half = 0;
+  ti.ghost = 0;
+  ti.swap = 0;
+  ti.tail_n = 0;
   if constexpr (KindTraits<KIND>::kTokenRows) {
-    const int mt = t / p.n_tiles;
-    const int nt = t - mt * p.n_tiles;
-    ti.m0 = mt * kBM;
+    const int nt_all = t / p.n_tiles;
+    const int nt = t - nt_all * p.n_tiles;
     ti.n0 = nt * (KIND == GemmKind::DA ? p.tile_n : KindTraits<KIND>::kTileN);
-    ti.e = find_segment(p.offsets, p.E, ti.m0);
+    if constexpr (KindTraits<KIND>::kPair) {
+      // nt_all is the pair index: expert e, pair j of it, this CTA's half l = 2j + rank
+      ti.e = find_segment_smem(pfx, p.E, nt_all);
+      const int beg = __ldg(p.offsets + ti.e);
+      const int mt = (__ldg(p.offsets + ti.e + 1) - beg) / kBM;
+      const int j = nt_all - pfx[ti.e];
+      // An odd last row tile has no partner tile: the pair computes it transposed
+      // (weights as the M = 256 operand, its token rows as N), so only its real rows,
+      // rounded up to 32, cost MMA time.  DA with 128-column tiles has no M = 256 form of
+      // the swap and runs the tile with an idle (ghost) odd half instead.
+      if ((mt & 1) && 2 * j + 1 == mt && (KIND != GemmKind::DA || p.tile_n == 256)) {
+        ti.swap = 1;
+        ti.m0 = beg + (mt - 1) * kBM;
+        int rows = kBM;
+        if (p.counts) {
+          rows = __ldg(p.counts + ti.e) - (mt - 1) * kBM;
+          rows = rows < 0 ? 0 : (rows > kBM ? kBM : rows);
+        }
+        ti.tail_n = rows <= 32 ? 32 : (rows + 31) & ~31;
+      } else {
+        const int l = 2 * j + rank;
+        ti.ghost = l >= mt;
+        ti.m0 = beg + l * kBM;   // a ghost reads rows past the expert (never stored)
+      }
+    } else {
+      ti.m0 = nt_all * kBM;
+      ti.e = find_segment(p.offsets, p.E, ti.m0);
+    }
     if constexpr (KIND == GemmKind::GateUp || KIND == GemmKind::BwdGU || KIND == GemmKind::DA)
       ti.nkb = p.D / kBK;
     if constexpr (KIND == GemmKind::Down) ti.nkb = p.I / kBK;
@@ -177,30 +285,107 @@ __device__ __forceinline__ void issue_kblock(const GemmParams& p, const TileInfo
   }
 }
 
-// Bytes one K block of a tile delivers to shared memory.
+// Pair kinds: this CTA's share of K block kb (its 128 rows of A, its half of B's columns);
+// completion is counted on the even CTA's full barrier `fb` (a shared::cluster address).
+template <GemmKind KIND>
+__device__ __forceinline__ void issue_kblock_pair(const GemmParams& p, const TileInfo& ti, int kb,
+                                                  uint32_t fb, uint8_t* sA, uint8_t* sB,
+                                                  int rank) {
+  const int k0 = kb * kBK;
+  tma_load_2d_pair(&p.mapA0, fb, sA, k0, ti.m0);
+  if constexpr (KIND == GemmKind::GateUp || KIND == GemmKind::BwdGU) {
+    // N = 128 gate columns (even CTA) | the same 128 up columns (odd CTA), two 64-wide atoms
+    tma_load_3d_pair(rank ? &p.mapB1 : &p.mapB0, fb, sB, 0, ti.e * p.D + k0, ti.n0 / 64);
+  } else if constexpr (KIND == GemmKind::DA) {
+    // W_d[e] feature rows, K-major: tile_n / 2 rows per CTA
+    tma_load_2d_pair(&p.mapB0, fb, sB, k0, ti.e * p.I + ti.n0 + rank * (p.tile_n / 2));
+  } else if constexpr (KIND == GemmKind::Down) {
+    tma_load_3d_pair(&p.mapB0, fb, sB, 0, ti.e * p.I + k0, ti.n0 / 64 + 2 * rank);
+  } else if constexpr (KIND == GemmKind::Dx) {
+    const int r = ti.e * p.D + ti.n0 + 128 * rank;
+    if (k0 < p.I) tma_load_2d_pair(&p.mapB0, fb, sB, k0, r);
+    else tma_load_2d_pair(&p.mapB1, fb, sB, k0 - p.I, r);
+  }
+}
+
+// Pair kinds, swapped tail tile: this CTA's 128 weight rows (the M operand: output
+// features, or for gate/up 64 gate + the same 64 up features) into sA, and its half of
+// the tail's token rows (the N operand; a fixed 64-row box, of which the MMA reads
+// tail_n / 2) into sB.
+template <GemmKind KIND>
+__device__ __forceinline__ void issue_kblock_swap(const GemmParams& p, const TileInfo& ti, int kb,
+                                                  uint32_t fb, uint8_t* sA, uint8_t* sB,
+                                                  int rank) {
+  const int k0 = kb * kBK;
+  tma_load_2d_pair(&p.mapA1, fb, sB, k0, ti.m0 + rank * (ti.tail_n / 2));
+  if constexpr (KIND == GemmKind::GateUp || KIND == GemmKind::BwdGU) {
+    const int atom = (ti.n0 + 64 * rank) / 64;
+    tma_load_3d_pair(&p.mapB2, fb, sA, 0, ti.e * p.D + k0, atom);          // gate, 1 atom
+    tma_load_3d_pair(&p.mapB3, fb, sA + 8192, 0, ti.e * p.D + k0, atom);   // up, 1 atom
+  } else if constexpr (KIND == GemmKind::DA) {
+    tma_load_2d_pair(&p.mapB0, fb, sA, k0, ti.e * p.I + ti.n0 + 128 * rank);
+  } else if constexpr (KIND == GemmKind::Down) {
+    tma_load_3d_pair(&p.mapB0, fb, sA, 0, ti.e * p.I + k0, ti.n0 / 64 + 2 * rank);
+  } else if constexpr (KIND == GemmKind::Dx) {
+    const int r = ti.e * p.D + ti.n0 + 128 * rank;
+    if (k0 < p.I) tma_load_2d_pair(&p.mapB0, fb, sA, k0, r);
+    else tma_load_2d_pair(&p.mapB1, fb, sA, k0 - p.I, r);
+  }
+}
+
+// Bytes one K block of a swapped tail delivers to each CTA: 128 weight rows + 64 token rows.
+constexpr uint32_t kSwapKBlockBytes = 16 * 1024 + 8 * 1024;
+
+// Bytes one K block of a tile delivers to this CTA's shared memory.
 template <GemmKind KIND>
 __device__ __forceinline__ uint32_t kblock_bytes(const GemmParams& p) {
+  if constexpr (KindTraits<KIND>::kPair) {
+    if constexpr (KIND == GemmKind::DA) return 16 * 1024 + static_cast<uint32_t>(p.tile_n) * 64;
+    return 32 * 1024;
+  }
   if constexpr (KIND == GemmKind::DA) return 16 * 1024 + static_cast<uint32_t>(p.tile_n) * 128;
   return 48 * 1024;
 }
 
 template <GemmKind KIND>
 __device__ __forceinline__ void produce(const GemmParams& p, GemmBarriers* bars, uint8_t* stages,
-                                        volatile int* abort) {
-  constexpr int S = KindTraits<KIND>::kStages;
+                                        const int* pfx, volatile int* abort) {
+  using Tr = KindTraits<KIND>;
+  constexpr int S = Tr::kStages;
   int stage = 0;
   uint32_t phase = 0;
-  const int ntiles = num_tiles<KIND>(p);
+  const int ntiles = num_tiles<KIND>(p, pfx);
   const uint32_t bytes = kblock_bytes<KIND>(p);
+  const int rank = Tr::kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const uint32_t full0 = Tr::kPair ? mapa_shared(smem_u32(&bars->full[0]), 0) : 0u;
   if (p.drop_loads) return;   // test hook: nothing arrives, the consumers' waits expire
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const TileInfo ti = decode_tile<KIND>(p, t);
+  for (int t = first_tile<KIND>(); t < ntiles; t += tile_stride<KIND>()) {
+    const TileInfo ti = decode_tile<KIND>(p, t, pfx, rank);
     for (int kb = 0; kb < ti.nkb; ++kb) {
       if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, p.err, kDevTimeoutProducer)) return;
-      uint8_t* sA = stages + stage * kStageBytes;
-      uint64_t* fb = &bars->full[stage];
-      mbar_arrive_expect_tx(fb, bytes);   // posted before the copies are issued
-      issue_kblock<KIND>(p, ti, kb, fb, sA, sA + kStageBOffset);
+      uint8_t* sA = stages + stage * Tr::kStageBytes;
+      if constexpr (Tr::kPair) {
+        // the even CTA's barrier counts both CTAs' bytes; expect_tx is posted by the even
+        // CTA alone (the odd CTA's bytes may land first: the phase cannot complete before
+        // the even CTA has arrived)
+        const uint32_t fb = full0 + 8u * static_cast<uint32_t>(stage);
+        if (rank == 0)
+          mbar_arrive_expect_tx(&bars->full[stage], 2 * (ti.swap ? kSwapKBlockBytes : bytes));
+        if (ti.swap) issue_kblock_swap<KIND>(p, ti, kb, fb, sA, sA + kStageBOffset, rank);
+        else issue_kblock_pair<KIND>(p, ti, kb, fb, sA, sA + kStageBOffset, rank);
+      } else {
+        uint64_t* fb = &bars->full[stage];
+        mbar_arrive_expect_tx(fb, bytes);   // posted before the copies are issued
+        issue_kblock<KIND>(p, ti, kb, fb, sA, sA + kStageBOffset);
+      }
+      if (++stage == S) { stage = 0; phase ^= 1u; }
+    }
+  }
+  if constexpr (Tr::kPair) {
+    // Wait until the MMA issuer has released every stage: its releases arrive on this
+    // CTA's barriers from the even CTA and must all have landed before the CTA exits.
+    for (int i = 0; i < S; ++i) {
+      if (!mbar_wait(&bars->empty[stage], phase ^ 1u, abort, p.err, kDevTimeoutProducer)) return;
       if (++stage == S) { stage = 0; phase ^= 1u; }
     }
   }
@@ -209,17 +394,24 @@ __device__ __forceinline__ void produce(const GemmParams& p, GemmBarriers* bars,
 // ------------------------------------------------------------------ MMA issuer
 template <GemmKind KIND>
 __device__ __forceinline__ void mma_issue(const GemmParams& p, GemmBarriers* bars,
-                                          uint8_t* stages, uint32_t tmem_base,
+                                          uint8_t* stages, uint32_t tmem_base, const int* pfx,
                                           volatile int* abort) {
   using Tr = KindTraits<KIND>;
   constexpr int S = Tr::kStages;
+  // on a pair only the even CTA issues; the odd CTA's MMA warp just owns its TMEM
+  if constexpr (Tr::kPair) {
+    if (cluster_ctarank() != 0) return;
+  }
   // operand majors: A K-major except the weight gradients (token rows are their K);
   // B MN-major except where the weights are read transposed (Dx, DA)
   constexpr bool kAmn = Tr::kIsDw;
   constexpr bool kBmn = !(KIND == GemmKind::Dx || KIND == GemmKind::DA);
   // the weight-gradient GEMMs read fp16 operands (they touch no weights); the rest bf16
   const int n_mma = (KIND == GemmKind::DA) ? p.tile_n : 256;
-  const uint32_t idesc = umma_idesc_f16kind(128, n_mma, kAmn, kBmn, Tr::kIsDw);
+  const uint32_t idesc = umma_idesc_f16kind(Tr::kPair ? 256 : 128, n_mma, kAmn, kBmn, Tr::kIsDw);
+  // swapped tails: weights (sA) as the M operand, token rows (sB, K-major) as N
+  const uint32_t w_lbo = Tr::kWeightsMN ? 8192u : 16u;
+  const uint32_t w_step = Tr::kWeightsMN ? 2048u : 32u;
   const uint32_t a_lbo = kAmn ? 8192u : 16u;
   const uint32_t a_step = kAmn ? 2048u : 32u;
   const uint32_t b_lbo = kBmn ? 8192u : 16u;
@@ -229,30 +421,53 @@ __device__ __forceinline__ void mma_issue(const GemmParams& p, GemmBarriers* bar
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
-  const int ntiles = num_tiles<KIND>(p);
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const TileInfo ti = decode_tile<KIND>(p, t);
+  const int ntiles = num_tiles<KIND>(p, pfx);
+  for (int t = first_tile<KIND>(); t < ntiles; t += tile_stride<KIND>()) {
+    const TileInfo ti = decode_tile<KIND>(p, t, pfx, 0);
     if (ti.nkb == 0) continue;
     if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort, p.err, kDevTimeoutMma)) return;
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+    const uint32_t idesc_swap =
+        umma_idesc_f16kind(256, ti.swap ? ti.tail_n : 32, Tr::kWeightsMN, false, false);
     for (int kb = 0; kb < ti.nkb; ++kb) {
       if (!mbar_wait(&bars->full[stage], phase, abort, p.err, kDevTimeoutMma)) return;
       tc_fence_after();
-      const uint32_t sa = smem_u32(stages + stage * kStageBytes);
+      const uint32_t sa = smem_u32(stages + stage * Tr::kStageBytes);
       const uint32_t sb = sa + kStageBOffset;
+      if (Tr::kPair && ti.swap) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t ad = umma_desc_sw128(sa + a_step * k, a_lbo, 1024u);
-        const uint64_t bd = umma_desc_sw128(sb + b_step * k, b_lbo, 1024u);
-        umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = umma_desc_sw128(sa + w_step * k, w_lbo, 1024u);
+          const uint64_t bd = umma_desc_sw128(sb + 32u * k, 16u, 1024u);
+          umma_bf16_pair(d_tmem, ad, bd, idesc_swap, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = umma_desc_sw128(sa + a_step * k, a_lbo, 1024u);
+          const uint64_t bd = umma_desc_sw128(sb + b_step * k, b_lbo, 1024u);
+          if constexpr (Tr::kPair) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          else umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        }
       }
-      umma_commit(&bars->empty[stage]);
+      if constexpr (Tr::kPair) umma_commit_pair(&bars->empty[stage], 0x3);
+      else umma_commit(&bars->empty[stage]);
       if (++stage == S) { stage = 0; phase ^= 1u; }
     }
-    umma_commit(&bars->tfull[acc]);
+    if constexpr (Tr::kPair) umma_commit_pair(&bars->tfull[acc], 0x3);
+    else umma_commit(&bars->tfull[acc]);
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
+  }
+  if constexpr (Tr::kPair) {
+    // Wait for both CTAs' epilogues to release both accumulators: the odd CTA's releases
+    // arrive on this CTA's barriers and must all have landed before the pair exits.
+    for (int i = 0; i < 2; ++i) {
+      if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1u, abort, p.err, kDevTimeoutMma)) return;
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
   }
 }
 
@@ -309,10 +524,238 @@ __device__ __forceinline__ uint32_t f16x2_residual(uint32_t packed, float v0, fl
   return pack_f16x2(v0 - hf.x, v1 - hf.y);
 }
 
+// ------------------------------------------------------------------ swapped tails
+// The accumulator of a swapped tile is transposed: TMEM lane = output column (feature),
+// TMEM column = token row.  Each lane of a warp holds one column for 32 consecutive rows;
+// these place element (row i, column lane) into a 32 x 32 box.
+// 16-bit, 64-byte swizzle (chunk c of row r at c ^ ((r>>1)&3)).
+__device__ __forceinline__ void stage_16_col(uint8_t* buf, int lane, const float (&v)[32],
+                                             bool fp16) {
+  const int c = lane >> 3;
+  const int off = (lane & 7) * 2;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint16_t h = fp16 ? __half_as_ushort(__float2half_rn(v[i]))
+                            : __bfloat16_as_ushort(__float2bfloat16_rn(v[i]));
+    *reinterpret_cast<uint16_t*>(buf + i * 64 + ((c ^ ((i >> 1) & 3)) << 4) + off) = h;
+  }
+}
+
+// fp32, 128-byte swizzle (chunk c of row r at c ^ (r&7)).
+__device__ __forceinline__ void stage_f32_col(uint8_t* buf, int lane, const float (&v)[32]) {
+  const int c = lane >> 2;
+  const int off = (lane & 3) * 4;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    *reinterpret_cast<float*>(buf + i * 128 + ((c ^ (i & 7)) << 4) + off) = v[i];
+}
+
+// v[i] <- v[i] - fp16(v[i]): what the fp16 copy of v left out.
+__device__ __forceinline__ void to_f16_residual(float (&v)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] -= __half2float(__float2half_rn(v[i]));
+}
+
+// A zeroed box in the next ring buffer.
+template <int NBUF, int BYTES>
+__device__ __forceinline__ uint8_t* stage_zero(uint8_t* stg, int& ring, int lane) {
+  uint8_t* buf = ring_next<NBUF, BYTES>(stg, ring, lane);
+  for (int b = lane; b < BYTES / 16; b += 32)
+    *reinterpret_cast<uint4*>(buf + 16 * b) = make_uint4(0u, 0u, 0u, 0u);
+  return buf;
+}
+
+// Zeros for the padding rows of a swapped tile that were not computed (tail_n .. 127),
+// 32 columns at x.
+__device__ __forceinline__ void store_zero_rows(const CUtensorMap* map, const uint8_t* zbuf, int x,
+                                                const TileInfo& ti, int lane) {
+  for (int y = ti.m0 + ti.tail_n; y < ti.m0 + kBM; y += 32) store_box(map, zbuf, x, y, lane, false);
+}
+
+// Epilogue of a swapped tail tile; returns false when a bounded wait gave up.
+// Down, Dx, DA: TMEM lanes 32q.. hold output columns n0 + 128*rank + 32q + lane.
+// GateUp, BwdGU: lanes 0-63 hold gate and lanes 64-127 up of the same 64 act columns
+// n0 + 64*rank + (0..63); the up warp of each 32 columns hands its values to the gate
+// warp through its staging buffer (two mbarriers per warp pair), and the gate warp
+// computes and stores every output.
+template <GemmKind KIND>
+__device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers* bars, uint8_t* stg,
+                                              uint8_t* stg_base, uint32_t tb, const TileInfo& ti,
+                                              int q, int lane, int rank, int& ring, uint32_t& xph,
+                                              volatile int* abort) {
+  using Tr = KindTraits<KIND>;
+  constexpr int R16 = Tr::kRing16;
+  const int nch = ti.tail_n / 32;
+  if constexpr (KIND == GemmKind::Down || KIND == GemmKind::Dx) {
+    const int x = ti.n0 + 128 * rank + 32 * q;
+    for (int j = 0; j < nch; ++j) {
+      uint32_t r[32];
+      tmem_ld32(tb + 32 * j, r);
+      tmem_ld_wait(r);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
+      stage_16_col(buf, lane, v, false);
+      store_box(&p.mapO0, buf, x, ti.m0 + 32 * j, lane, false);
+    }
+    if (ti.tail_n < kBM)
+      store_zero_rows(&p.mapO0, stage_zero<R16, 2048>(stg, ring, lane), x, ti, lane);
+    return true;
+  } else if constexpr (KIND == GemmKind::DA) {
+    constexpr int R32 = Tr::kRing32;
+    const int x = ti.n0 + 128 * rank + 32 * q;
+    for (int j = 0; j < nch; ++j) {
+      const float wl = __ldg(p.w_perm + ti.m0 + 32 * j + lane);   // router weight of row lane
+      uint32_t r[32];
+      tmem_ld32(tb + 32 * j, r);
+      tmem_ld_wait(r);
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __shfl_sync(0xffffffffu, wl, i) * __uint_as_float(r[i]);
+      uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
+      stage_f32_col(buf, lane, v);
+      store_box(&p.mapO0, buf, x, ti.m0 + 32 * j, lane, false);
+    }
+    if (ti.tail_n < kBM)
+      store_zero_rows(&p.mapO0, stage_zero<R32, 4096>(stg, ring, lane), x, ti, lane);
+    return true;
+  } else {
+    const int pi = q & 1;
+    float* xbuf = reinterpret_cast<float*>(stg_base + pi * Tr::kEpiBytes);
+    if (q >= 2) {   // up warp
+      if (lane == 0) bulk_wait_read<0>();   // its staging is now the exchange buffer
+      __syncwarp();
+      for (int j = 0; j < nch; ++j) {
+        int ok = 1;
+        if (lane == 0)
+          ok = mbar_wait(&bars->xempty[pi], xph ^ 1u, abort, p.err, kDevTimeoutEpilogue);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return false;
+        uint32_t r[32];
+        tmem_ld32(tb + 32 * j, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xbuf[i * 32 + lane] = __uint_as_float(r[i]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->xfull[pi]);
+        xph ^= 1u;
+      }
+      return true;
+    }
+    // gate warp: act columns f0 .. f0+31
+    const int f0 = ti.n0 + 64 * rank + 32 * pi;
+    bool want_lo = false;
+    if constexpr (KIND == GemmKind::BwdGU)
+      want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
+    for (int j = 0; j < nch; ++j) {
+      const int row0 = ti.m0 + 32 * j;
+      uint32_t g[32];
+      tmem_ld32(tb + 32 * j, g);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&bars->xfull[pi], xph, abort, p.err, kDevTimeoutEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      tmem_ld_wait(g);
+      if (!ok) return false;
+      float u[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) u[i] = xbuf[i * 32 + lane];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->xempty[pi]);
+      xph ^= 1u;
+      float v[32];
+      if constexpr (KIND == GemmKind::GateUp) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gv = __uint_as_float(g[i]);
+          v[i] = gv * sigmoidf_fast(gv) * u[i];
+        }
+        uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(buf, lane, v, false);
+        store_box(&p.mapO0, buf, f0, row0, lane, false);
+      } else {
+        const float wl = __ldg(p.w_perm + row0 + lane);
+        const float* da = p.dA + static_cast<size_t>(row0) * p.I + f0 + lane;
+        float d[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) d[i] = __ldg(da + static_cast<size_t>(i) * p.I);
+        // w * act (fp16; dW_down operand)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gv = __uint_as_float(g[i]);
+          v[i] = __shfl_sync(0xffffffffu, wl, i) * gv * sigmoidf_fast(gv) * u[i];
+        }
+        uint8_t* b0 = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(b0, lane, v, true);
+        store_box(&p.mapO0, b0, f0, row0, lane, false);
+        if (want_lo) {
+          to_f16_residual(v);
+          uint8_t* c0 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_col(c0, lane, v, true);
+          store_box(&p.mapO3, c0, f0, row0, lane, false);
+        }
+        // dG = dA U silu'(G)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gv = __uint_as_float(g[i]);
+          const float sg = sigmoidf_fast(gv);
+          v[i] = d[i] * u[i] * sg * (1.0f + gv * (1.0f - sg));
+        }
+        uint8_t* b1 = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(b1, lane, v, false);
+        store_box(&p.mapO1, b1, f0, row0, lane, false);
+        uint8_t* b2 = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(b2, lane, v, true);
+        store_box(&p.mapO2, b2, f0, row0, lane, false);
+        if (want_lo) {
+          to_f16_residual(v);
+          uint8_t* c1 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_col(c1, lane, v, true);
+          store_box(&p.mapO4, c1, f0, row0, lane, false);
+        }
+        // dU = dA silu(G)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gv = __uint_as_float(g[i]);
+          v[i] = d[i] * gv * sigmoidf_fast(gv);
+        }
+        uint8_t* b3 = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(b3, lane, v, false);
+        store_box(&p.mapO1, b3, p.I + f0, row0, lane, false);
+        uint8_t* b4 = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(b4, lane, v, true);
+        store_box(&p.mapO2, b4, p.I + f0, row0, lane, false);
+        if (want_lo) {
+          to_f16_residual(v);
+          uint8_t* c2 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_col(c2, lane, v, true);
+          store_box(&p.mapO4, c2, p.I + f0, row0, lane, false);
+        }
+      }
+    }
+    if (ti.tail_n < kBM) {
+      const uint8_t* z = stage_zero<R16, 2048>(stg, ring, lane);
+      store_zero_rows(&p.mapO0, z, f0, ti, lane);
+      if constexpr (KIND == GemmKind::BwdGU) {
+        store_zero_rows(&p.mapO1, z, f0, ti, lane);
+        store_zero_rows(&p.mapO1, z, p.I + f0, ti, lane);
+        store_zero_rows(&p.mapO2, z, f0, ti, lane);
+        store_zero_rows(&p.mapO2, z, p.I + f0, ti, lane);
+        if (want_lo) {
+          store_zero_rows(&p.mapO3, z, f0, ti, lane);
+          store_zero_rows(&p.mapO4, z, f0, ti, lane);
+          store_zero_rows(&p.mapO4, z, p.I + f0, ti, lane);
+        }
+      }
+    }
+    return true;
+  }
+}
+
 // ------------------------------------------------------------------ epilogue
 template <GemmKind KIND>
 __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars, uint8_t* stg,
-                                         uint32_t tmem_base, int warp, int lane,
+                                         uint32_t tmem_base, const int* pfx, int warp, int lane,
                                          volatile int* abort) {
   using Tr = KindTraits<KIND>;
   constexpr int R16 = Tr::kRing16;
@@ -321,9 +764,14 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
   int ring = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
-  const int ntiles = num_tiles<KIND>(p);
-  for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const TileInfo ti = decode_tile<KIND>(p, t);
+  const int rank = Tr::kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  // accumulator releases go to the even CTA, whose MMA issuer waits on them
+  const uint32_t tempty0 = Tr::kPair ? mapa_shared(smem_u32(&bars->tempty[0]), 0) : 0u;
+  uint8_t* stg_base = stg - (warp - 2) * Tr::kEpiBytes;
+  uint32_t xph = 0;   // swapped gate/up tails: exchange phase of this warp's pair
+  const int ntiles = num_tiles<KIND>(p, pfx);
+  for (int t = first_tile<KIND>(); t < ntiles; t += tile_stride<KIND>()) {
+    const TileInfo ti = decode_tile<KIND>(p, t, pfx, rank);
     const int row = ti.m0 + 32 * q;   // first of this warp's 32 rows; lane owns row + lane
     if constexpr (Tr::kIsDw) {
       if (ti.nkb == 0) {  // expert without tokens: its weight gradient is exactly zero
@@ -353,147 +801,160 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                         static_cast<uint32_t>(acc * 256);
 
-    if constexpr (KIND == GemmKind::GateUp) {
-      for (int c = 0; c < 4; ++c) {
-        uint32_t g[32], u[32];
-        tmem_ld32(tb + 32 * c, g);
-        tmem_ld32(tb + 128 + 32 * c, u);
-        tmem_ld_wait(g);
-        tmem_ld_after_wait(u);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float a[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float gv = __uint_as_float(g[2 * i + h]);
-            a[h] = gv * sigmoidf_fast(gv) * __uint_as_float(u[2 * i + h]);
+    bool swapped = false;
+    if constexpr (Tr::kPair) {
+      if (ti.swap) {
+        if (!epilogue_swap<KIND>(p, bars, stg, stg_base, tb, ti, q, lane, rank, ring, xph, abort))
+          return;
+        swapped = true;
+      }
+    }
+    if (!swapped && !ti.ghost) {   // a ghost half only drains its accumulator
+      if constexpr (KIND == GemmKind::GateUp) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tb + 32 * c, g);
+          tmem_ld32(tb + 128 + 32 * c, u);
+          tmem_ld_wait(g);
+          tmem_ld_after_wait(u);
+          uint32_t pk[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float a[2];
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float gv = __uint_as_float(g[2 * i + h]);
+              a[h] = gv * sigmoidf_fast(gv) * __uint_as_float(u[2 * i + h]);
+            }
+            pk[i] = pack_bf16x2(a[0], a[1]);
           }
-          pk[i] = pack_bf16x2(a[0], a[1]);
+          uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(buf, lane, pk);
+          store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
         }
-        uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(buf, lane, pk);
-        store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
-      }
-    } else if constexpr (KIND == GemmKind::Down || KIND == GemmKind::Dx) {
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tb + 32 * c, r);
-        tmem_ld_wait(r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-        uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(buf, lane, pk);
-        store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
-      }
-    } else if constexpr (KIND == GemmKind::DA) {
-      const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
-      const int nch = p.tile_n / 32;
-      for (int c = 0; c < nch; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tb + 32 * c, r);
-        tmem_ld_wait(r);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = wr * __uint_as_float(r[i]);
-        uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
-        stage_f32_row(buf, lane, v);
-        store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
-      }
-    } else if constexpr (KIND == GemmKind::BwdGU) {
-      const int my_row = row + lane;
-      const float wr = __ldg(p.w_perm + my_row);
-      // rows of an expert whose dW is split over several tiles also get the fp16 residuals
-      const bool want_lo =
-          (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
-      const float4* da_row =
-          reinterpret_cast<const float4*>(p.dA + static_cast<size_t>(my_row) * p.I + ti.n0);
-      for (int c = 0; c < 4; ++c) {
-        float4 d4[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d4[i] = __ldg(da_row + 8 * c + i);   // w-scaled dA, fp32
-        uint32_t g[32], u[32];
-        tmem_ld32(tb + 32 * c, g);
-        tmem_ld32(tb + 128 + 32 * c, u);
-        tmem_ld_wait(g);
-        tmem_ld_after_wait(u);
-        const float* da = reinterpret_cast<const float*>(d4);
-        uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16], la[16], lg[16], lu[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float r[2][3];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float gv = __uint_as_float(g[2 * i + h]);
-            const float uv = __uint_as_float(u[2 * i + h]);
-            const float dv = da[2 * i + h];
-            const float sg = sigmoidf_fast(gv);
-            const float si = gv * sg;
-            r[h][0] = wr * si * uv;                              // w * act (dW_down operand)
-            r[h][1] = dv * uv * sg * (1.0f + gv * (1.0f - sg));  // dG
-            r[h][2] = dv * si;                                   // dU
+      } else if constexpr (KIND == GemmKind::Down || KIND == GemmKind::Dx) {
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + 32 * c, r);
+          tmem_ld_wait(r);
+          uint32_t pk[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(buf, lane, pk);
+          store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
+        }
+      } else if constexpr (KIND == GemmKind::DA) {
+        const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
+        const int nch = p.tile_n / 32;
+        for (int c = 0; c < nch; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + 32 * c, r);
+          tmem_ld_wait(r);
+          float v[32];
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = wr * __uint_as_float(r[i]);
+          uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
+          stage_f32_row(buf, lane, v);
+          store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
+        }
+      } else if constexpr (KIND == GemmKind::BwdGU) {
+        const int my_row = row + lane;
+        const float wr = __ldg(p.w_perm + my_row);
+        // rows of an expert whose dW is split over several tiles also get the fp16 residuals
+        const bool want_lo =
+            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
+        const float4* da_row =
+            reinterpret_cast<const float4*>(p.dA + static_cast<size_t>(my_row) * p.I + ti.n0);
+        for (int c = 0; c < 4; ++c) {
+          float4 d4[8];
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) d4[i] = __ldg(da_row + 8 * c + i);   // w-scaled dA, fp32
+          uint32_t g[32], u[32];
+          tmem_ld32(tb + 32 * c, g);
+          tmem_ld32(tb + 128 + 32 * c, u);
+          tmem_ld_wait(g);
+          tmem_ld_after_wait(u);
+          const float* da = reinterpret_cast<const float*>(d4);
+          uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16], la[16], lg[16], lu[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float r[2][3];
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float gv = __uint_as_float(g[2 * i + h]);
+              const float uv = __uint_as_float(u[2 * i + h]);
+              const float dv = da[2 * i + h];
+              const float sg = sigmoidf_fast(gv);
+              const float si = gv * sg;
+              r[h][0] = wr * si * uv;                              // w * act (dW_down operand)
+              r[h][1] = dv * uv * sg * (1.0f + gv * (1.0f - sg));  // dG
+              r[h][2] = dv * si;                                   // dU
+            }
+            pa[i] = pack_f16x2(r[0][0], r[1][0]);
+            pg[i] = pack_bf16x2(r[0][1], r[1][1]);
+            pu[i] = pack_bf16x2(r[0][2], r[1][2]);
+            pg16[i] = pack_f16x2(r[0][1], r[1][1]);
+            pu16[i] = pack_f16x2(r[0][2], r[1][2]);
+            la[i] = f16x2_residual(pa[i], r[0][0], r[1][0]);
+            lg[i] = f16x2_residual(pg16[i], r[0][1], r[1][1]);
+            lu[i] = f16x2_residual(pu16[i], r[0][2], r[1][2]);
           }
-          pa[i] = pack_f16x2(r[0][0], r[1][0]);
-          pg[i] = pack_bf16x2(r[0][1], r[1][1]);
-          pu[i] = pack_bf16x2(r[0][2], r[1][2]);
-          pg16[i] = pack_f16x2(r[0][1], r[1][1]);
-          pu16[i] = pack_f16x2(r[0][2], r[1][2]);
-          la[i] = f16x2_residual(pa[i], r[0][0], r[1][0]);
-          lg[i] = f16x2_residual(pg16[i], r[0][1], r[1][1]);
-          lu[i] = f16x2_residual(pu16[i], r[0][2], r[1][2]);
+          const int col = ti.n0 + 32 * c;
+          uint8_t* b0 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(b0, lane, pa);
+          store_box(&p.mapO0, b0, col, row, lane, false);        // w*act, fp16
+          uint8_t* b1 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(b1, lane, pg);
+          store_box(&p.mapO1, b1, col, row, lane, false);        // dG, bf16
+          uint8_t* b2 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(b2, lane, pu);
+          store_box(&p.mapO1, b2, p.I + col, row, lane, false);  // dU, bf16
+          uint8_t* b3 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(b3, lane, pg16);
+          store_box(&p.mapO2, b3, col, row, lane, false);        // dG, fp16
+          uint8_t* b4 = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(b4, lane, pu16);
+          store_box(&p.mapO2, b4, p.I + col, row, lane, false);  // dU, fp16
+          if (want_lo) {
+            uint8_t* c0 = ring_next<R16, 2048>(stg, ring, lane);
+            stage_16_row(c0, lane, la);
+            store_box(&p.mapO3, c0, col, row, lane, false);        // w*act residual
+            uint8_t* c1 = ring_next<R16, 2048>(stg, ring, lane);
+            stage_16_row(c1, lane, lg);
+            store_box(&p.mapO4, c1, col, row, lane, false);        // dG residual
+            uint8_t* c2 = ring_next<R16, 2048>(stg, ring, lane);
+            stage_16_row(c2, lane, lu);
+            store_box(&p.mapO4, c2, p.I + col, row, lane, false);  // dU residual
+          }
         }
-        const int col = ti.n0 + 32 * c;
-        uint8_t* b0 = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(b0, lane, pa);
-        store_box(&p.mapO0, b0, col, row, lane, false);        // w*act, fp16
-        uint8_t* b1 = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(b1, lane, pg);
-        store_box(&p.mapO1, b1, col, row, lane, false);        // dG, bf16
-        uint8_t* b2 = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(b2, lane, pu);
-        store_box(&p.mapO1, b2, p.I + col, row, lane, false);  // dU, bf16
-        uint8_t* b3 = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(b3, lane, pg16);
-        store_box(&p.mapO2, b3, col, row, lane, false);        // dG, fp16
-        uint8_t* b4 = ring_next<R16, 2048>(stg, ring, lane);
-        stage_16_row(b4, lane, pu16);
-        store_box(&p.mapO2, b4, p.I + col, row, lane, false);  // dU, fp16
-        if (want_lo) {
-          uint8_t* c0 = ring_next<R16, 2048>(stg, ring, lane);
-          stage_16_row(c0, lane, la);
-          store_box(&p.mapO3, c0, col, row, lane, false);        // w*act residual
-          uint8_t* c1 = ring_next<R16, 2048>(stg, ring, lane);
-          stage_16_row(c1, lane, lg);
-          store_box(&p.mapO4, c1, col, row, lane, false);        // dG residual
-          uint8_t* c2 = ring_next<R16, 2048>(stg, ring, lane);
-          stage_16_row(c2, lane, lu);
-          store_box(&p.mapO4, c2, p.I + col, row, lane, false);  // dU residual
-        }
-      }
-    } else {  // DwGU, DwD: fp32 out, plain store or split-K reduce-add
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tb + 32 * c, r);
-        tmem_ld_wait(r);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
-        stage_f32_row(buf, lane, v);
-        const int col = ti.n0 + 32 * c;
-        if (KIND == GemmKind::DwGU) {
-          if (col < p.I) store_box(&p.mapO0, buf, col, ti.e * p.D + row, lane, ti.split);
-          else store_box(&p.mapO1, buf, col - p.I, ti.e * p.D + row, lane, ti.split);
-        } else {
-          store_box(&p.mapO0, buf, col, ti.e * p.I + row, lane, ti.split);
+      } else {  // DwGU, DwD: fp32 out, plain store or split-K reduce-add
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tb + 32 * c, r);
+          tmem_ld_wait(r);
+          float v[32];
+  #pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
+          stage_f32_row(buf, lane, v);
+          const int col = ti.n0 + 32 * c;
+          if (KIND == GemmKind::DwGU) {
+            if (col < p.I) store_box(&p.mapO0, buf, col, ti.e * p.D + row, lane, ti.split);
+            else store_box(&p.mapO1, buf, col - p.I, ti.e * p.D + row, lane, ti.split);
+          } else {
+            store_box(&p.mapO0, buf, col, ti.e * p.I + row, lane, ti.split);
+          }
         }
       }
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->tempty[acc]);
+    if (lane == 0) {
+      if constexpr (Tr::kPair) mbar_arrive_cluster(tempty0 + 8u * static_cast<uint32_t>(acc));
+      else mbar_arrive(&bars->tempty[acc]);
+    }
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
   }
@@ -504,11 +965,13 @@ template <GemmKind KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1) k_grouped_gemm(const __grid_constant__ GemmParams p) {
   using Tr = KindTraits<KIND>;
   extern __shared__ uint8_t smem_raw[];
+  // identical offsets in both CTAs of a pair: the even CTA's descriptors address both
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   GemmBarriers* bars = reinterpret_cast<GemmBarriers*>(smem);
   uint8_t* stages = smem + 1024;
-  uint8_t* staging = stages + Tr::kStages * kStageBytes;
+  uint8_t* staging = stages + Tr::kStages * Tr::kStageBytes;
+  int* pfx = reinterpret_cast<int*>(staging + kEpiWarps * Tr::kEpiBytes);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -521,7 +984,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_grouped_gemm(const __grid_c
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->tfull[i], 1);
-      mbar_init(&bars->tempty[i], kEpiWarps);
+      // a pair's accumulators are released by the epilogue warps of both CTAs
+      mbar_init(&bars->tempty[i], Tr::kPair ? 2 * kEpiWarps : kEpiWarps);
+      mbar_init(&bars->xfull[i], 1);
+      mbar_init(&bars->xempty[i], 1);
     }
     bars->abort = 0;
     fence_mbarrier_init();
@@ -530,21 +996,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_grouped_gemm(const __grid_c
     tma_prefetch_desc(&p.mapA0);
     tma_prefetch_desc(&p.mapB0);
   }
+  if constexpr (Tr::kPair) build_pair_prefix(p, pfx);   // contains a __syncthreads
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_addr, kTmemCols);
-    tmem_relinquish();
+    if constexpr (Tr::kPair) {
+      tmem_alloc_pair(&bars->tmem_addr, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&bars->tmem_addr, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before any copy or arrival targets them
+  if constexpr (Tr::kPair) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_addr;
 
   if (warp == 0) {
-    if (lane == 0) produce<KIND>(p, bars, stages, abort);
+    if (lane == 0) produce<KIND>(p, bars, stages, pfx, abort);
   } else if (warp == 1) {
-    if (lane == 0) mma_issue<KIND>(p, bars, stages, tmem_base, abort);
+    if (lane == 0) mma_issue<KIND>(p, bars, stages, tmem_base, pfx, abort);
   } else {
-    epilogue<KIND>(p, bars, staging + (warp - 2) * Tr::kEpiBytes, tmem_base, warp, lane, abort);
+    epilogue<KIND>(p, bars, staging + (warp - 2) * Tr::kEpiBytes, tmem_base, pfx, warp, lane,
+                   abort);
     if (lane == 0) bulk_wait_all();
   }
 
@@ -557,30 +1032,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1) k_grouped_gemm(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair frees TMEM or exits while the other may still reach its memory
+  if constexpr (Tr::kPair) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (Tr::kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
+// `max_tiles` bounds the device-side tile count (pair kinds: pair tiles).
 template <GemmKind KIND>
 cudaError_t launch_gemm_kind(const GemmParams& p, int max_tiles, int num_sms, cudaStream_t s) {
-  constexpr int kSmem = KindTraits<KIND>::kSmemBytes;
+  using Tr = KindTraits<KIND>;
+  constexpr int kSmem = Tr::kSmemBytes;
   static_assert(kSmem <= 232448, "shared memory budget");
   static bool configured[64] = {};
+  static int max_pairs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm<KIND>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  int grid = max_tiles < num_sms ? max_tiles : num_sms;
-  if (grid < 1) grid = 1;
-  k_grouped_gemm<KIND><<<grid, kGemmThreads, kSmem, s>>>(p);
-  return cudaGetLastError();
+  if constexpr (Tr::kPair) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_pairs[dev] == 0) {
+      // pairs that fit on the GPU at once (clusters are placed within a GPC)
+      cfg.gridDim = dim3(2 * (num_sms / 2));
+      int n = 0;
+      cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_grouped_gemm<KIND>, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorInvalidConfiguration;
+      max_pairs[dev] = n;
+    }
+    int pairs = max_tiles < max_pairs[dev] ? max_tiles : max_pairs[dev];
+    if (pairs < 1) pairs = 1;
+    cfg.gridDim = dim3(2 * pairs);
+    return cudaLaunchKernelEx(&cfg, k_grouped_gemm<KIND>, p);
+  } else {
+    int grid = max_tiles < num_sms ? max_tiles : num_sms;
+    if (grid < 1) grid = 1;
+    k_grouped_gemm<KIND><<<grid, kGemmThreads, kSmem, s>>>(p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace moe

@@ -54,6 +54,7 @@ enum class GemmKind : int { GateUp = 0, Down = 1, DA = 2, BwdGU = 3, Dx = 4, DwG
 constexpr int kBM = 128;        // token rows (or feature rows for dW) per tile
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kDwChunkRows = 2048;  // tokens per dW split-K chunk
+constexpr int kMaxExperts = 1024;   // largest E the entry points accept
 
 struct GemmParams {
   CUtensorMap mapA0;
@@ -61,12 +62,14 @@ struct GemmParams {
   CUtensorMap mapB0;
   CUtensorMap mapB1;
   CUtensorMap mapB2;
+  CUtensorMap mapB3;
   CUtensorMap mapO0;
   CUtensorMap mapO1;
   CUtensorMap mapO2;
   CUtensorMap mapO3;
   CUtensorMap mapO4;
   const int* offsets;      // [E+1] padded expert offsets (device)
+  const int* counts;       // [E] real rows per expert (device) or null: all rows are real
   const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
   const float* w_perm;     // [cap] router weight per sorted row (DA, BwdGU)
   const float* dA;         // [cap, I] router-weighted dA, fp32 (BwdGU reads it)

@@ -160,7 +160,7 @@ static bool map_store_f32(CUtensorMap* m, const void* b, uint64_t inner, uint64_
 
 // ------------------------------------------------------------------ sizes
 static bool basic_sizes_ok(int T, int K, int E, int align) {
-  if (T < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || align < 1) return false;
+  if (T < 0 || K < 1 || K > 32 || E < 1 || E > kMaxExperts || align < 1) return false;
   const long long R = static_cast<long long>(T) * K;
   const long long cap = R + static_cast<long long>(E) * (align - 1) + align;
   return R < (1ll << 31) && cap < (1ll << 31);
@@ -309,8 +309,9 @@ MOE_EXPORT int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm,
 
 MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_gate,
                                   const moe_bf16_t* w_up, const moe_bf16_t* w_down,
-                                  const int32_t* offsets, int T, int K, int E, int D, int I,
-                                  int align, moe_bf16_t* y_perm, void* workspace, void* stream) {
+                                  const int32_t* offsets, const int32_t* counts, int T, int K,
+                                  int E, int D, int I, int align, moe_bf16_t* y_perm,
+                                  void* workspace, void* stream) {
   if (!basic_sizes_ok(T, K, E, align)) return MOE_ERR_INVALID_ARG;
   if (!gemm_shape_ok(D, I, align)) return MOE_ERR_UNSUPPORTED;
   if (!x_perm || !w_gate || !w_up || !w_down || !offsets || !y_perm || !workspace)
@@ -326,16 +327,22 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   const uint64_t cap = capacity_of(T, K, E, align);
   void* act = ws + L.act;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int m_tiles_max = static_cast<int>(cap / kBM);
+  // token-row GEMMs run on CTA pairs: at most (row tiles + E) / 2 pairs of 256 rows
+  const int pairs_max = static_cast<int>((cap / kBM + E + 1) / 2);
 
   GemmParams p{};
   p.offsets = offsets;
+  p.counts = counts;
   p.err = reinterpret_cast<int*>(ws);
   p.E = E; p.D = D; p.I = I;
-  // gate/up + SwiGLU
+  // gate/up + SwiGLU (A1, B2, B3: the token rows and one-atom weight boxes of the
+  // swapped tail tiles)
   bool ok = map_kmajor(&p.mapA0, x_perm, D, cap, 128) &&
+            map_kmajor(&p.mapA1, x_perm, D, cap, 64) &&
             map_mnmajor(&p.mapB0, w_gate, I, static_cast<uint64_t>(E) * D, 2) &&
             map_mnmajor(&p.mapB1, w_up, I, static_cast<uint64_t>(E) * D, 2) &&
+            map_mnmajor(&p.mapB2, w_gate, I, static_cast<uint64_t>(E) * D, 1) &&
+            map_mnmajor(&p.mapB3, w_up, I, static_cast<uint64_t>(E) * D, 1) &&
             map_store_16(&p.mapO0, act, I, cap);
   if (!ok) return MOE_ERR_CUDA;
   p.n_tiles = I / 128;
@@ -343,29 +350,31 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   cudaError_t e;
   {
     LaunchScope ls(kKGemmGateUp, s);
-    e = launch_gemm_kind<GemmKind::GateUp>(p, m_tiles_max * p.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::GateUp>(p, pairs_max * p.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   // down projection
   GemmParams q{};
   q.offsets = offsets;
+  q.counts = counts;
   q.err = p.err;
   q.E = E; q.D = D; q.I = I;
-  ok = map_kmajor(&q.mapA0, act, I, cap, 128) &&
-       map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I, 4) &&
+  ok = map_kmajor(&q.mapA0, act, I, cap, 128) && map_kmajor(&q.mapA1, act, I, cap, 64) &&
+       map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I, 2) &&
        map_store_16(&q.mapO0, y_perm, D, cap);
   if (!ok) return MOE_ERR_CUDA;
   q.n_tiles = D / 256;
   {
     LaunchScope ls(kKGemmDown, s);
-    e = launch_gemm_kind<GemmKind::Down>(q, m_tiles_max * q.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::Down>(q, pairs_max * q.n_tiles, f->num_sms, s);
   }
   return to_status(e);
 }
 
 MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm,
                                   const int32_t* perm_src, const float* w_perm,
-                                  const int32_t* offsets, const moe_bf16_t* w_gate,
+                                  const int32_t* offsets, const int32_t* counts,
+                                  const moe_bf16_t* w_gate,
                                   const moe_bf16_t* w_up, const moe_bf16_t* w_down, int T, int K,
                                   int E, int D, int I, int align, moe_bf16_t* dx_perm,
                                   float* dw_gate, float* dw_up, float* dw_down, void* workspace,
@@ -391,7 +400,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   void* dh = ws + L.dh;
   moe_bf16_t* dyp = reinterpret_cast<moe_bf16_t*>(ws + L.dyp);
   int* dw_prefix = reinterpret_cast<int*>(ws + L.dw_prefix);
-  const int m_tiles_max = static_cast<int>(cap / kBM);
+  const int pairs_max = static_cast<int>((cap / kBM + E + 1) / 2);
   const uint64_t ED = static_cast<uint64_t>(E) * D, EI = static_cast<uint64_t>(E) * I;
   cudaError_t e;
 
@@ -410,22 +419,25 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   // 2. dA = w * dy_perm W_d^T (fp32), then the gate/up recompute with the SwiGLU' epilogue
   float* dA = reinterpret_cast<float*>(ws + L.da);
   GemmParams da{};
-  da.offsets = offsets; da.w_perm = w_perm; da.err = err; da.E = E; da.D = D; da.I = I;
+  da.offsets = offsets; da.counts = counts; da.w_perm = w_perm; da.err = err;
+  da.E = E; da.D = D; da.I = I;
   da.tile_n = (I % 256 == 0) ? 256 : 128;
-  bool ok = map_kmajor(&da.mapA0, dyp, D, cap, 128) &&
-            map_kmajor(&da.mapB0, w_down, D, EI, static_cast<uint32_t>(da.tile_n)) &&
+  bool ok = map_kmajor(&da.mapA0, dyp, D, cap, 128) && map_kmajor(&da.mapA1, dyp, D, cap, 64) &&
+            map_kmajor(&da.mapB0, w_down, D, EI, static_cast<uint32_t>(da.tile_n / 2)) &&
             map_store_f32(&da.mapO0, dA, I, cap);
   if (!ok) return MOE_ERR_CUDA;
   da.n_tiles = I / da.tile_n;
   {
     LaunchScope ls(kKGemmDA, s);
-    e = launch_gemm_kind<GemmKind::DA>(da, m_tiles_max * da.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::DA>(da, pairs_max * da.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams a{};
-  a.offsets = offsets; a.w_perm = w_perm; a.dA = dA; a.err = err; a.E = E; a.D = D; a.I = I;
-  ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) &&
+  a.offsets = offsets; a.counts = counts; a.w_perm = w_perm; a.dA = dA; a.err = err;
+  a.E = E; a.D = D; a.I = I;
+  ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) && map_kmajor(&a.mapA1, x_perm, D, cap, 64) &&
        map_mnmajor(&a.mapB0, w_gate, I, ED, 2) && map_mnmajor(&a.mapB1, w_up, I, ED, 2) &&
+       map_mnmajor(&a.mapB2, w_gate, I, ED, 1) && map_mnmajor(&a.mapB3, w_up, I, ED, 1) &&
        map_store_16(&a.mapO0, act, I, cap, Elem::F16) &&
        map_store_16(&a.mapO1, dh, 2ull * I, cap) &&
        map_store_16(&a.mapO2, dh16, 2ull * I, cap, Elem::F16) &&
@@ -435,20 +447,21 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   a.n_tiles = I / 128;
   {
     LaunchScope ls(kKGemmBwdGU, s);
-    e = launch_gemm_kind<GemmKind::BwdGU>(a, m_tiles_max * a.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::BwdGU>(a, pairs_max * a.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 3. input gradient
   GemmParams x{};
-  x.offsets = offsets; x.err = err; x.E = E; x.D = D; x.I = I;
-  ok = map_kmajor(&x.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&x.mapB0, w_gate, I, ED, 256) &&
-       map_kmajor(&x.mapB1, w_up, I, ED, 256) && map_store_16(&x.mapO0, dx_perm, D, cap);
+  x.offsets = offsets; x.counts = counts; x.err = err; x.E = E; x.D = D; x.I = I;
+  ok = map_kmajor(&x.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&x.mapA1, dh, 2ull * I, cap, 64) &&
+       map_kmajor(&x.mapB0, w_gate, I, ED, 128) &&
+       map_kmajor(&x.mapB1, w_up, I, ED, 128) && map_store_16(&x.mapO0, dx_perm, D, cap);
   if (!ok) return MOE_ERR_CUDA;
   x.n_tiles = D / 256;
   {
     LaunchScope ls(kKGemmDx, s);
-    e = launch_gemm_kind<GemmKind::Dx>(x, m_tiles_max * x.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::Dx>(x, pairs_max * x.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

@@ -16,9 +16,14 @@ from . import binding as B
 
 
 class MoEExpertMLP:
+    """`skip_padding`: pass the routing's per-expert counts to the GEMMs so that they
+    compute only the real rows of each expert's last row tile (rounded up to 32); off,
+    every padded row is computed.  The results are the same either way."""
+
     def __init__(self, T: int, K: int, E: int, D: int, I: int, align: int = 128,
-                 device: str | torch.device = "cuda"):
+                 device: str | torch.device = "cuda", skip_padding: bool = True):
         self.T, self.K, self.E, self.D, self.I, self.align = T, K, E, D, I, align
+        self.skip_padding = skip_padding
         dev = torch.device(device)
         self.device = dev
         self.cap = B.moe_capacity(T, K, E, align)
@@ -50,8 +55,8 @@ class MoEExpertMLP:
         B.moe_route_permute(topk_ids, topk_w, x, T, K, E, D, a, self.counts, self.offsets,
                             self.perm_src, self.inv_perm, self.w_perm, self.x_perm,
                             self.workspace, stream)
-        B.moe_expert_mlp_fwd(self.x_perm, w_gate, w_up, w_down, self.offsets, T, K, E, D, I, a,
-                             self.y_perm, self.workspace, stream)
+        B.moe_expert_mlp_fwd(self.x_perm, w_gate, w_up, w_down, self.offsets, self._counts(), T,
+                             K, E, D, I, a, self.y_perm, self.workspace, stream)
         B.moe_combine(self.y_perm, self.inv_perm, topk_w, T, K, D, self.y, stream)
         return self.y
 
@@ -59,11 +64,14 @@ class MoEExpertMLP:
         """(dX [T,D] bf16, dW_gate [E,D,I] f32, dW_up [E,D,I] f32, dW_down [E,I,D] f32)
         of L = sum(Y * dy), for the routing of the last forward."""
         T, K, E, D, I, a = self.T, self.K, self.E, self.D, self.I, self.align
-        B.moe_expert_mlp_bwd(dy, self.x_perm, self.perm_src, self.w_perm, self.offsets, w_gate,
-                             w_up, w_down, T, K, E, D, I, a, self.dx_perm, self.dw_gate,
-                             self.dw_up, self.dw_down, self.workspace, stream)
+        B.moe_expert_mlp_bwd(dy, self.x_perm, self.perm_src, self.w_perm, self.offsets,
+                             self._counts(), w_gate, w_up, w_down, T, K, E, D, I, a, self.dx_perm,
+                             self.dw_gate, self.dw_up, self.dw_down, self.workspace, stream)
         B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, self.dx, stream)
         return self.dx, self.dw_gate, self.dw_up, self.dw_down
+
+    def _counts(self):
+        return self.counts if self.skip_padding else None
 
     def device_error(self, stream=None):
         return B.moe_get_device_error(self.workspace, stream)

@@ -34,7 +34,7 @@ def test_library_is_sm103a_only():
 
 
 def test_abi_version_and_status_strings(lib):
-    assert B.moe_abi_version() == 1
+    assert B.moe_abi_version() == 2
     assert B.moe_status_string(0) == "ok"
     assert "invalid" in B.moe_status_string(-1)
     assert B.moe_status_string(12345) == "unknown status"
@@ -60,15 +60,18 @@ def test_invalid_sizes_rejected_on_host(lib):
     st = L.moe_combine(nul, nul, nul, 4, 2, 250, nul, nul)   # D not a multiple of 8
     assert st == B.MOE_ERR_INVALID_ARG
     # GEMM shapes the kernels do not tile are reported as unsupported
-    st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, 8, 2, 4, 200, 128, 128, nul, nul, nul)
+    st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, nul, 8, 2, 4, 200, 128, 128, nul, nul,
+                              nul)
     assert st == B.MOE_ERR_UNSUPPORTED
-    st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 64, nul, nul, nul)
+    st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 64, nul, nul,
+                              nul)
     assert st == B.MOE_ERR_UNSUPPORTED
-    st = L.moe_expert_mlp_bwd(nul, nul, nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 96, 128,
-                              nul, nul, nul, nul, nul, nul)
+    st = L.moe_expert_mlp_bwd(nul, nul, nul, nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 96,
+                              128, nul, nul, nul, nul, nul, nul)
     assert st == B.MOE_ERR_UNSUPPORTED
     # null buffers are rejected
-    st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 128, nul, nul, nul)
+    st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 128, nul, nul,
+                              nul)
     assert st == B.MOE_ERR_INVALID_ARG
 
 

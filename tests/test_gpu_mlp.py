@@ -104,6 +104,41 @@ def test_small_layers(T, D, I, E, K, seed):
     check_full(random_layer(T, D, I, E, K, seed), T, D, I, E, K)
 
 
+@pytest.mark.parametrize("I", [256, 384])
+def test_tail_tile_sizes(I):
+    """Experts whose last row tile has 1, 31, 32, 33, 127, 128 real rows (one tile), 129
+    (two tiles) and 300 (three): every odd last tile is computed transposed over its real
+    rows rounded up to 32, the rest of it written as zeros.  With I = 384 the dA GEMM has
+    128-column tiles and runs those tiles with an idle CTA half instead."""
+    counts = [1, 31, 32, 33, 127, 128, 129, 300, 0]
+    E, K, D = len(counts), 1, 256
+    T = sum(counts)
+    ids = torch.cat([torch.full((c, 1), e, dtype=torch.int32) for e, c in enumerate(counts)])
+    ids = ids[torch.randperm(T, generator=torch.Generator().manual_seed(3))]
+    check_full(random_layer(T, D, I, E, K, seed=12, ids=ids), T, D, I, E, K)
+
+
+def test_padding_skip_changes_nothing():
+    """The GEMMs given the real row counts produce exactly what they produce computing
+    every padded row (padding rows of the inputs are zero)."""
+    T, D, I, E, K = 700, 512, 256, 6, 2
+    g = {k: v.to(DEV) for k, v in random_layer(T, D, I, E, K, seed=11).items()}
+    outs = []
+    for skip in (True, False):
+        layer = MoEExpertMLP(T, K, E, D, I, align=128, device=DEV, skip_padding=skip)
+        layer.forward(g["x"], g["topk_ids"], g["topk_w"], g["w_gate"], g["w_up"], g["w_down"])
+        layer.backward(g["dy"], g["w_gate"], g["w_up"], g["w_down"])
+        torch.cuda.synchronize()
+        assert layer.device_error()[0] == B.MOE_OK
+        outs.append([t.clone() for t in (layer.y_perm, layer.y, layer.dx_perm, layer.dx,
+                                          layer.dw_gate, layer.dw_up, layer.dw_down)])
+    used = int(layer.offsets[-1])
+    for name, a, b in zip(("y_perm", "y", "dx_perm", "dx", "dW_gate", "dW_up", "dW_down"), *outs):
+        if name.endswith("_perm"):
+            a, b = a[:used], b[:used]
+        assert torch.equal(a, b), name
+
+
 def test_split_expert_reduce_add():
     """One expert holds 5000 rows (> 2048): its weight gradient is split into three
     token chunks that are TMA reduce-added; the other experts are empty or small."""
