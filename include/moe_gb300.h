@@ -142,7 +142,8 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  * Expert MLP backward on the sorted rows ("LigerMoE design / Backward pass"):
  *   1. routed expert-output gradient: the rows dy[perm_src[s] / K] (zero on padding); the
  *      router weight w_perm[s] is applied in fp32 inside step 2
- *   2. recompute G = x_perm W_gate[e], U = x_perm W_up[e]; dA = w_perm[s] * dy_row W_down[e]^T;
+ *   2. recompute G = x_perm W_gate[e], U = x_perm W_up[e]; dA = w_perm[s] * dy_row W_down[e]^T
+ *      (fp32, kept in fp16);
  *      dG = dA U silu'(G), dU = dA silu(G)  (bf16 for step 3, fp16 copies for step 4),
  *      and w_perm[s] * silu(G) U (fp16, for step 4)
  *   3. input gradient  dx_perm[s] = bf16( dG[s] W_gate[e]^T + dU[s] W_up[e]^T )
@@ -154,12 +155,16 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *      over several tiles whose parts are TMA reduce-added.  Experts with no rows get
  *      exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
  *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets/counts (counts may be NULL) from
- *   moe_route_permute, weights as in the forward -- all device.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
+ *   moe_route_permute, weights as in the forward -- all device.  x [T,D] bf16 (device) or
+ *   NULL: the unsorted input of the forward; when given, step 4's fp16 copy of the sorted
+ *   rows is gathered from it (each token row is read K times, mostly from cache) instead
+ *   of being read from x_perm.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
  *   dw_gate [E,D,I] fp32, dw_up [E,D,I] fp32, dw_down [E,I,D] fp32 (fully overwritten).
  * Reduce dx_perm to tokens with moe_combine(dx_perm, inv_perm, NULL, ...).
  * Needs D % 256 == 0, I % 128 == 0, align % 128 == 0.
  */
-int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm, const int32_t* perm_src,
+int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x, const moe_bf16_t* x_perm,
+                       const int32_t* perm_src,
                        const float* w_perm, const int32_t* offsets, const int32_t* counts,
                        const moe_bf16_t* w_gate, const moe_bf16_t* w_up,
                        const moe_bf16_t* w_down, int T, int K, int E, int D, int I, int align,

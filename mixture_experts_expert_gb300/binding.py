@@ -45,7 +45,7 @@ _SIGS = {
     "moe_route_permute": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_mlp_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
-    "moe_expert_mlp_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+    "moe_expert_mlp_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _P, _P, _P, _P, _P, _P]),
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), _P]),
     "moe_route_permute_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
@@ -180,12 +180,12 @@ def moe_combine(src_perm, inv_perm, topk_w, T, K, D, out, stream=None):
     _check("moe_combine", st)
 
 
-def moe_expert_mlp_bwd(dy, x_perm, perm_src, w_perm, offsets, counts, w_gate, w_up, w_down, T,
-                       K, E, D, I, align, dx_perm, dw_gate, dw_up, dw_down, workspace,
+def moe_expert_mlp_bwd(dy, x, x_perm, perm_src, w_perm, offsets, counts, w_gate, w_up, w_down,
+                       T, K, E, D, I, align, dx_perm, dw_gate, dw_up, dw_down, workspace,
                        stream=None):
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     st = lib().moe_expert_mlp_bwd(
-        _ptr(dy, bf, "dy", T == 0), _ptr(x_perm, bf, "x_perm"), _ptr(perm_src, i32, "perm_src"),
+        _ptr(dy, bf, "dy", T == 0), _ptr(x, bf, "x", True), _ptr(x_perm, bf, "x_perm"), _ptr(perm_src, i32, "perm_src"),
         _ptr(w_perm, f32, "w_perm"), _ptr(offsets, i32, "offsets"),
         _ptr(counts, i32, "counts", True), _ptr(w_gate, bf, "w_gate"),
         _ptr(w_up, bf, "w_up"), _ptr(w_down, bf, "w_down"), T, K, E, D, I, align,

@@ -25,7 +25,8 @@
 // Kinds (row-major; "perm" rows are expert-sorted, padded to 128 rows per expert):
 //   GateUp  act[s, i]  = silu(x_perm[s] W_g[e])_i * (x_perm[s] W_u[e])_i   N: 128 gate + 128 up
 //   Down    y_perm[s]  = act[s] W_d[e]
-//   DA      dA[s]      = w_perm[s] * dy_perm[s] W_d[e]^T        (fp32 out; dy_perm unscaled)
+//   DA      dA[s]      = w_perm[s] * dy_perm[s] W_d[e]^T   (scaled in fp32, stored fp16; dy_perm
+//           unscaled); for experts split over several dW tiles also the fp16 residual
 //   BwdGU   recompute G, U as GateUp; the epilogue reads dA and writes w*act (fp16),
 //           dG = dA U silu'(G), dU = dA silu(G) (bf16 for Dx, fp16 for the dW GEMMs) and,
 //           for experts split over several dW tiles, the fp16 residuals v - fp16(v)
@@ -75,9 +76,8 @@ struct KindTraits {
   // Every kind is load-latency bound, so stages take what the epilogue staging leaves
   // (for the single-CTA kinds three stages measured slower than four even for the
   // write-heavy weight-gradient GEMMs, given a deeper store ring).
-  static constexpr int kStages = !kPair ? 4 : (KIND == GemmKind::DA ? 5 : 6);
-  static constexpr int kEpiBytes =                                   // staging per epilogue warp
-      !kPair ? 8 * 1024 : (KIND == GemmKind::DA ? 12 * 1024 : 6 * 1024);
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kEpiBytes = kPair ? 6 * 1024 : 8 * 1024;      // staging per epilogue warp
   static constexpr int kRing16 = kEpiBytes / 2048;                   // 2 KB 16-bit boxes
   static constexpr int kRing32 = kEpiBytes / 4096;                   // 4 KB fp32 boxes
   // pair kinds: per-expert prefix of row pairs, [0, E]
@@ -603,8 +603,8 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
       store_zero_rows(&p.mapO0, stage_zero<R16, 2048>(stg, ring, lane), x, ti, lane);
     return true;
   } else if constexpr (KIND == GemmKind::DA) {
-    constexpr int R32 = Tr::kRing32;
     const int x = ti.n0 + 128 * rank + 32 * q;
+    const bool want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
     for (int j = 0; j < nch; ++j) {
       const float wl = __ldg(p.w_perm + ti.m0 + 32 * j + lane);   // router weight of row lane
       uint32_t r[32];
@@ -613,12 +613,21 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __shfl_sync(0xffffffffu, wl, i) * __uint_as_float(r[i]);
-      uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
-      stage_f32_col(buf, lane, v);
+      uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
+      stage_16_col(buf, lane, v, true);
       store_box(&p.mapO0, buf, x, ti.m0 + 32 * j, lane, false);
+      if (want_lo) {
+        to_f16_residual(v);
+        uint8_t* lb = ring_next<R16, 2048>(stg, ring, lane);
+        stage_16_col(lb, lane, v, true);
+        store_box(&p.mapO1, lb, x, ti.m0 + 32 * j, lane, false);
+      }
     }
-    if (ti.tail_n < kBM)
-      store_zero_rows(&p.mapO0, stage_zero<R32, 4096>(stg, ring, lane), x, ti, lane);
+    if (ti.tail_n < kBM) {
+      const uint8_t* z = stage_zero<R16, 2048>(stg, ring, lane);
+      store_zero_rows(&p.mapO0, z, x, ti, lane);
+      if (want_lo) store_zero_rows(&p.mapO1, z, x, ti, lane);
+    }
     return true;
   } else {
     const int pi = q & 1;
@@ -675,10 +684,19 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
         store_box(&p.mapO0, buf, f0, row0, lane, false);
       } else {
         const float wl = __ldg(p.w_perm + row0 + lane);
-        const float* da = p.dA + static_cast<size_t>(row0) * p.I + f0 + lane;
+        const unsigned short* da = reinterpret_cast<const unsigned short*>(p.dA) +
+                                   static_cast<size_t>(row0) * p.I + f0 + lane;
         float d[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) d[i] = __ldg(da + static_cast<size_t>(i) * p.I);
+        for (int i = 0; i < 32; ++i)
+          d[i] = __half2float(__ushort_as_half(__ldg(da + static_cast<size_t>(i) * p.I)));
+        if (want_lo) {   // dA's fp16 residual, kept for the experts split over dW tiles
+          const unsigned short* dl = reinterpret_cast<const unsigned short*>(p.dA_lo) +
+                                     static_cast<size_t>(row0) * p.I + f0 + lane;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            d[i] += __half2float(__ushort_as_half(__ldg(dl + static_cast<size_t>(i) * p.I)));
+        }
         // w * act (fp16; dW_down operand)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -847,17 +865,29 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         }
       } else if constexpr (KIND == GemmKind::DA) {
         const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
+        const bool want_lo =
+            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
         const int nch = p.tile_n / 32;
         for (int c = 0; c < nch; ++c) {
           uint32_t r[32];
           tmem_ld32(tb + 32 * c, r);
           tmem_ld_wait(r);
-          float v[32];
+          uint32_t pk[16], lo[16];
   #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = wr * __uint_as_float(r[i]);
-          uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
-          stage_f32_row(buf, lane, v);
+          for (int i = 0; i < 16; ++i) {
+            const float v0 = wr * __uint_as_float(r[2 * i]);
+            const float v1 = wr * __uint_as_float(r[2 * i + 1]);
+            pk[i] = pack_f16x2(v0, v1);
+            lo[i] = f16x2_residual(pk[i], v0, v1);
+          }
+          uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
+          stage_16_row(buf, lane, pk);
           store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
+          if (want_lo) {   // the fp16 residual, for experts split over dW tiles
+            uint8_t* lb = ring_next<R16, 2048>(stg, ring, lane);
+            stage_16_row(lb, lane, lo);
+            store_box(&p.mapO1, lb, ti.n0 + 32 * c, row, lane, false);
+          }
         }
       } else if constexpr (KIND == GemmKind::BwdGU) {
         const int my_row = row + lane;
@@ -865,18 +895,42 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         // rows of an expert whose dW is split over several tiles also get the fp16 residuals
         const bool want_lo =
             (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
-        const float4* da_row =
-            reinterpret_cast<const float4*>(p.dA + static_cast<size_t>(my_row) * p.I + ti.n0);
+        const uint4* da_row =
+            reinterpret_cast<const uint4*>(p.dA + static_cast<size_t>(my_row) * p.I + ti.n0);
+        const uint4* dl_row =
+            reinterpret_cast<const uint4*>(p.dA_lo + static_cast<size_t>(my_row) * p.I + ti.n0);
         for (int c = 0; c < 4; ++c) {
-          float4 d4[8];
+          uint4 d4[4], l4[4];
   #pragma unroll
-          for (int i = 0; i < 8; ++i) d4[i] = __ldg(da_row + 8 * c + i);   // w-scaled dA, fp32
+          for (int i = 0; i < 4; ++i) d4[i] = __ldg(da_row + 4 * c + i);   // w-scaled dA, fp16
+          if (want_lo) {
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) l4[i] = __ldg(dl_row + 4 * c + i);   // its residual
+          }
           uint32_t g[32], u[32];
           tmem_ld32(tb + 32 * c, g);
           tmem_ld32(tb + 128 + 32 * c, u);
           tmem_ld_wait(g);
           tmem_ld_after_wait(u);
-          const float* da = reinterpret_cast<const float*>(d4);
+          float da[32];
+          {
+            const __half2* h2 = reinterpret_cast<const __half2*>(d4);
+  #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 f = __half22float2(h2[i]);
+              da[2 * i] = f.x;
+              da[2 * i + 1] = f.y;
+            }
+            if (want_lo) {
+              const __half2* l2 = reinterpret_cast<const __half2*>(l4);
+  #pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float2 f = __half22float2(l2[i]);
+                da[2 * i] += f.x;
+                da[2 * i + 1] += f.y;
+              }
+            }
+          }
           uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16], la[16], lg[16], lu[16];
   #pragma unroll
           for (int i = 0; i < 16; ++i) {

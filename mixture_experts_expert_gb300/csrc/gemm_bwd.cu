@@ -1,4 +1,4 @@
-// Backward grouped GEMMs on token rows: dA (router-weighted, fp32), the gate/up
+// Backward grouped GEMMs on token rows: dA (router-weighted, fp16), the gate/up
 // recompute with the fused SwiGLU' epilogue, and the input gradient.
 #include "gemm.cuh"
 

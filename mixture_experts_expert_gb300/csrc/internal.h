@@ -72,7 +72,8 @@ struct GemmParams {
   const int* counts;       // [E] real rows per expert (device) or null: all rows are real
   const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
   const float* w_perm;     // [cap] router weight per sorted row (DA, BwdGU)
-  const float* dA;         // [cap, I] router-weighted dA, fp32 (BwdGU reads it)
+  const uint16_t* dA;      // [cap, I] router-weighted dA, fp16 (BwdGU reads it)
+  const uint16_t* dA_lo;   // [cap, I] its fp16 residual (rows of experts split over dW tiles)
   int* err;                // device error word
   int E, D, I;
   int n_tiles;             // N tiles per M tile
@@ -97,8 +98,8 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, con
 
 // Backward operand preparation for every sorted row s < offsets[E]:
 //   dy_perm[s] = dy[perm_src[s] / K] (bf16, unscaled), dy16[s] = fp16 of the same row,
-//   x16[s] = fp16(x_perm[s]); zero rows on padding.
-cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x_perm,
+//   x16[s] = fp16(x[perm_src[s] / K]) (from x_perm[s] when x is null); zero rows on padding.
+cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
                                  const int32_t* perm_src, const int32_t* offsets, int E, int K,
                                  int D, int cap, uint16_t* dy_perm, uint16_t* dy16,
                                  uint16_t* x16, cudaStream_t s);

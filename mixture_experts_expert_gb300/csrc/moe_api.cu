@@ -175,13 +175,14 @@ static size_t capacity_of(int T, int K, int E, int align) {
 static size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 
 struct WsLayout {
-  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, da, total;
+  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, da, da_lo,
+      total;
 };
 
 // header | routing chunk counters | dW split prefix | act | dH | dy_perm | dH fp16 |
 // dy_perm fp16 | x_perm fp16 | w*act fp16 residual | dH fp16 residual (the residuals
 // are written only for experts whose weight gradient is split over several tiles) |
-// router-weighted dA fp32
+// router-weighted dA fp16 | its fp16 residual (split experts only)
 static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   WsLayout L;
   const size_t cap = capacity_of(T, K, E, align);
@@ -208,7 +209,9 @@ static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   L.dh16_lo = o;
   o = up1k(o + cap * static_cast<size_t>(I) * 4);
   L.da = o;
-  o = up1k(o + cap * static_cast<size_t>(I) * 4);
+  o = up1k(o + cap * static_cast<size_t>(I) * 2);
+  L.da_lo = o;
+  o = up1k(o + cap * static_cast<size_t>(I) * 2);
   L.total = o;
   return L;
 }
@@ -371,7 +374,8 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   return to_status(e);
 }
 
-MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm,
+MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
+                                  const moe_bf16_t* x_perm,
                                   const int32_t* perm_src, const float* w_perm,
                                   const int32_t* offsets, const int32_t* counts,
                                   const moe_bf16_t* w_gate,
@@ -386,7 +390,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
       !aligned16(dx_perm) || !aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down) ||
-      !aligned16(workspace) || (dy && !aligned16(dy)))
+      !aligned16(workspace) || (dy && !aligned16(dy)) || (x && !aligned16(x)))
     return MOE_ERR_INVALID_ARG;
   int st = check_device();
   if (st != MOE_OK) return st;
@@ -412,19 +416,22 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
 
   // 1. routed expert-output gradient rows (unscaled; the router weight is applied to dA in
   //    fp32) and the fp16 operand copies of the weight-gradient GEMMs
-  e = launch_bwd_prep_rows(dy, x_perm, perm_src, offsets, E, K, D, static_cast<int>(cap), dyp,
+  e = launch_bwd_prep_rows(dy, x, x_perm, perm_src, offsets, E, K, D, static_cast<int>(cap), dyp,
                            dyp16, xp16, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
-  // 2. dA = w * dy_perm W_d^T (fp32), then the gate/up recompute with the SwiGLU' epilogue
-  float* dA = reinterpret_cast<float*>(ws + L.da);
+  // 2. dA = w * dy_perm W_d^T (scaled in fp32, kept in fp16), then the gate/up recompute
+  //    with the SwiGLU' epilogue
+  uint16_t* dA = reinterpret_cast<uint16_t*>(ws + L.da);
+  uint16_t* dA_lo = reinterpret_cast<uint16_t*>(ws + L.da_lo);
   GemmParams da{};
   da.offsets = offsets; da.counts = counts; da.w_perm = w_perm; da.err = err;
   da.E = E; da.D = D; da.I = I;
   da.tile_n = (I % 256 == 0) ? 256 : 128;
   bool ok = map_kmajor(&da.mapA0, dyp, D, cap, 128) && map_kmajor(&da.mapA1, dyp, D, cap, 64) &&
             map_kmajor(&da.mapB0, w_down, D, EI, static_cast<uint32_t>(da.tile_n / 2)) &&
-            map_store_f32(&da.mapO0, dA, I, cap);
+            map_store_16(&da.mapO0, dA, I, cap, Elem::F16) &&
+            map_store_16(&da.mapO1, dA_lo, I, cap, Elem::F16);
   if (!ok) return MOE_ERR_CUDA;
   da.n_tiles = I / da.tile_n;
   {
@@ -433,7 +440,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams a{};
-  a.offsets = offsets; a.counts = counts; a.w_perm = w_perm; a.dA = dA; a.err = err;
+  a.offsets = offsets; a.counts = counts; a.w_perm = w_perm; a.dA = dA; a.dA_lo = dA_lo;
+  a.err = err;
   a.E = E; a.D = D; a.I = I;
   ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) && map_kmajor(&a.mapA1, x_perm, D, cap, 64) &&
        map_mnmajor(&a.mapB0, w_gate, I, ED, 2) && map_mnmajor(&a.mapB1, w_up, I, ED, 2) &&
@@ -452,16 +460,16 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x_perm
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 3. input gradient
-  GemmParams x{};
-  x.offsets = offsets; x.counts = counts; x.err = err; x.E = E; x.D = D; x.I = I;
-  ok = map_kmajor(&x.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&x.mapA1, dh, 2ull * I, cap, 64) &&
-       map_kmajor(&x.mapB0, w_gate, I, ED, 128) &&
-       map_kmajor(&x.mapB1, w_up, I, ED, 128) && map_store_16(&x.mapO0, dx_perm, D, cap);
+  GemmParams xg{};
+  xg.offsets = offsets; xg.counts = counts; xg.err = err; xg.E = E; xg.D = D; xg.I = I;
+  ok = map_kmajor(&xg.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&xg.mapA1, dh, 2ull * I, cap, 64) &&
+       map_kmajor(&xg.mapB0, w_gate, I, ED, 128) &&
+       map_kmajor(&xg.mapB1, w_up, I, ED, 128) && map_store_16(&xg.mapO0, dx_perm, D, cap);
   if (!ok) return MOE_ERR_CUDA;
-  x.n_tiles = D / 256;
+  xg.n_tiles = D / 256;
   {
     LaunchScope ls(kKGemmDx, s);
-    e = launch_gemm_kind<GemmKind::Dx>(x, pairs_max * x.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::Dx>(xg, pairs_max * xg.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 

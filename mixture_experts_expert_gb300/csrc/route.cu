@@ -263,7 +263,8 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 q) {
 // For every sorted row s < offsets[E]: dy_perm[s] = dy[perm_src[s]/K] (bf16 copy),
 // dy16[s] = the same row in fp16, x16[s] = fp16(x_perm[s]); zero rows on padding.
 __global__ void __launch_bounds__(256) k_bwd_prep_rows(
-    const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x_perm,
+    const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
+    const uint16_t* __restrict__ x_perm,
     const int32_t* __restrict__ perm_src, const int32_t* __restrict__ offsets, int E, int K,
     int D, uint16_t* __restrict__ dy_perm, uint16_t* __restrict__ dy16,
     uint16_t* __restrict__ x16) {
@@ -277,7 +278,6 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     uint4* dp = reinterpret_cast<uint4*>(dy_perm + off);
     uint4* d16 = reinterpret_cast<uint4*>(dy16 + off);
     uint4* x16p = reinterpret_cast<uint4*>(x16 + off);
-    const uint4* xp = reinterpret_cast<const uint4*>(x_perm + off);
     if (j < 0) {
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int v = lane; v < nvec; v += 32) {
@@ -287,7 +287,10 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
       }
       continue;
     }
-    const uint4* sp = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(j / K) * D);
+    const size_t tok = static_cast<size_t>(j / K) * D;
+    const uint4* sp = reinterpret_cast<const uint4*>(dy + tok);
+    // the token's row of x (read K times, from cache) when given, else the sorted copy
+    const uint4* xp = reinterpret_cast<const uint4*>(x ? x + tok : x_perm + off);
     for (int v = lane; v < nvec; v += 32) {
       const uint4 q = __ldg(sp + v);
       const uint4 xq = __ldg(xp + v);
@@ -298,15 +301,15 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
   }
 }
 
-cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x_perm,
+cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
                                  const int32_t* perm_src, const int32_t* offsets, int E, int K,
                                  int D, int cap, uint16_t* dy_perm, uint16_t* dy16,
                                  uint16_t* x16, cudaStream_t s) {
   int blocks = (cap + 7) / 8;
   if (blocks < 1) blocks = 1;
   LaunchScope ls(kKBwdPrepRows, s);
-  k_bwd_prep_rows<<<blocks, 256, 0, s>>>(dy, x_perm, perm_src, offsets, E, K, D, dy_perm, dy16,
-                                         x16);
+  k_bwd_prep_rows<<<blocks, 256, 0, s>>>(dy, x, x_perm, perm_src, offsets, E, K, D, dy_perm,
+                                         dy16, x16);
   return cudaGetLastError();
 }
 

@@ -66,8 +66,8 @@ def test_invalid_sizes_rejected_on_host(lib):
     st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 64, nul, nul,
                               nul)
     assert st == B.MOE_ERR_UNSUPPORTED
-    st = L.moe_expert_mlp_bwd(nul, nul, nul, nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 96,
-                              128, nul, nul, nul, nul, nul, nul)
+    st = L.moe_expert_mlp_bwd(nul, nul, nul, nul, nul, nul, nul, nul, nul, nul, 8, 2, 4, 256,
+                              96, 128, nul, nul, nul, nul, nul, nul)
     assert st == B.MOE_ERR_UNSUPPORTED
     # null buffers are rejected
     st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 128, nul, nul,

@@ -139,6 +139,22 @@ def test_padding_skip_changes_nothing():
         assert torch.equal(a, b), name
 
 
+def test_backward_without_unsorted_x():
+    """Without the unsorted x the backward reads its fp16 copy of the sorted rows from
+    x_perm: the same values, so the same results bit for bit."""
+    T, D, I, E, K = 300, 256, 256, 4, 2
+    g = {k: v.to(DEV) for k, v in random_layer(T, D, I, E, K, seed=13).items()}
+    layer = MoEExpertMLP(T, K, E, D, I, align=128, device=DEV)
+    layer.forward(g["x"], g["topk_ids"], g["topk_w"], g["w_gate"], g["w_up"], g["w_down"])
+    ref = [t.clone() for t in layer.backward(g["dy"], g["w_gate"], g["w_up"], g["w_down"])]
+    layer._x = None
+    out = layer.backward(g["dy"], g["w_gate"], g["w_up"], g["w_down"])
+    torch.cuda.synchronize()
+    assert layer.device_error()[0] == B.MOE_OK
+    for a, b in zip(ref, out):
+        assert torch.equal(a, b)
+
+
 def test_split_expert_reduce_add():
     """One expert holds 5000 rows (> 2048): its weight gradient is split into three
     token chunks that are TMA reduce-added; the other experts are empty or small."""
