@@ -232,9 +232,16 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, cons
     const int beg = __ldg(p.offsets + ti.e);
     const int end = __ldg(p.offsets + ti.e + 1);
     ti.row0 = beg + j * kDwChunkRows;
-    int rows = end - ti.row0;
+    // K runs over the chunk's rows up to the expert's last real row (with counts) rounded
+    // up to 64: the padding rows after it are zero in every operand
+    int last = end;
+    if (p.counts) {
+      const int real = beg + __ldg(p.counts + ti.e);
+      last = real < end ? real : end;
+    }
+    int rows = last - ti.row0;
     rows = rows < kDwChunkRows ? rows : kDwChunkRows;
-    ti.nkb = rows > 0 ? rows / kBK : 0;
+    ti.nkb = rows > 0 ? (rows + kBK - 1) / kBK : 0;
     ti.split = nch > 1;
     ti.kb_half = ti.nkb;
     if (ti.split) ti.nkb *= 2;   // compensated operands: the value pass, then the residual pass
@@ -792,6 +799,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
     const TileInfo ti = decode_tile<KIND>(p, t, pfx, rank);
     const int row = ti.m0 + 32 * q;   // first of this warp's 32 rows; lane owns row + lane
     if constexpr (Tr::kIsDw) {
+      if (ti.nkb == 0 && ti.split) continue;   // a chunk without real rows adds nothing
       if (ti.nkb == 0) {  // expert without tokens: its weight gradient is exactly zero
         float z[32];
 #pragma unroll

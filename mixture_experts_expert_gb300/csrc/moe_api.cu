@@ -478,7 +478,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int max_chunks = E + static_cast<int>(cap / kDwChunkRows) + 1;
   GemmParams g{};
-  g.offsets = offsets; g.dw_prefix = dw_prefix; g.err = err; g.E = E; g.D = D; g.I = I;
+  g.offsets = offsets; g.counts = counts; g.dw_prefix = dw_prefix; g.err = err;
+  g.E = E; g.D = D; g.I = I;
   ok = map_mnmajor(&g.mapA0, xp16, D, cap, 2, Elem::F16) &&
        map_mnmajor(&g.mapB0, dh16, 2ull * I, cap, 4, Elem::F16) &&
        map_mnmajor(&g.mapB1, dh16_lo, 2ull * I, cap, 4, Elem::F16) &&
@@ -492,7 +493,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams d{};
-  d.offsets = offsets; d.dw_prefix = dw_prefix; d.err = err; d.E = E; d.D = D; d.I = I;
+  d.offsets = offsets; d.counts = counts; d.dw_prefix = dw_prefix; d.err = err;
+  d.E = E; d.D = D; d.I = I;
   ok = map_mnmajor(&d.mapA0, act, I, cap, 2, Elem::F16) &&
        map_mnmajor(&d.mapA1, act_lo, I, cap, 2, Elem::F16) &&
        map_mnmajor(&d.mapB0, dyp16, D, cap, 4, Elem::F16) &&
