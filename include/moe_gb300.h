@@ -233,6 +233,10 @@ long long moe_launch_count(long long* counts);
  */
 int moe_timing_enable(int on);
 
+/* The same for the kernels whose bit (1 << id) is set in kernel_mask only (0 = off), so
+ * that timing one kernel adds two events per launch of it and nothing elsewhere. */
+int moe_timing_enable_mask(unsigned long long kernel_mask);
+
 /* Waits for the recorded events, adds each launch's duration to ms[id] and 1 to
  * launches[id] (arrays of moe_num_kernels() entries, zeroed by the caller), and
  * forgets the records. */

@@ -55,6 +55,7 @@ _SIGS = {
     "moe_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_launch_count": (ctypes.c_longlong, [ctypes.POINTER(ctypes.c_longlong)]),
     "moe_timing_enable": (_I, [_I]),
+    "moe_timing_enable_mask": (_I, [ctypes.c_ulonglong]),
     "moe_timing_collect": (_I, [ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -224,6 +225,15 @@ def moe_launch_count():
 
 def moe_timing_enable(on: bool):
     _check("moe_timing_enable", lib().moe_timing_enable(1 if on else 0))
+
+
+def moe_timing_enable_only(names):
+    """Times only the named kernels (an empty list turns timing off)."""
+    ids = kernel_names()
+    mask = 0
+    for n in names:
+        mask |= 1 << ids.index(n)
+    _check("moe_timing_enable_mask", lib().moe_timing_enable_mask(mask))
 
 
 def moe_timing_collect():

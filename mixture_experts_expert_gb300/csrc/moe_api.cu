@@ -26,7 +26,7 @@ namespace {
 std::atomic<long long> g_launch_total{0};
 std::atomic<long long> g_launch_by_id[kNumKernelIds];
 std::mutex g_timing_mu;
-bool g_timing = false;
+std::atomic<unsigned long long> g_timing_mask{0};   // bit id: bracket kernel id with events
 struct TimingRec {
   int id;
   cudaEvent_t a, b;
@@ -49,7 +49,7 @@ cudaEvent_t pool_event() {
 LaunchScope::LaunchScope(int id_, cudaStream_t s) : id(id_), stream(s), slot(-1) {
   g_launch_total.fetch_add(1, std::memory_order_relaxed);
   if (id >= 0 && id < kNumKernelIds) g_launch_by_id[id].fetch_add(1, std::memory_order_relaxed);
-  if (g_timing) {
+  if (id >= 0 && id < kNumKernelIds && ((g_timing_mask.load() >> id) & 1ull)) {
     std::lock_guard<std::mutex> lk(g_timing_mu);
     TimingRec r{id, pool_event(), pool_event()};
     cudaEventRecord(r.a, s);
@@ -543,8 +543,12 @@ MOE_EXPORT long long moe_launch_count(long long* counts) {
 }
 
 MOE_EXPORT int moe_timing_enable(int on) {
-  std::lock_guard<std::mutex> lk(g_timing_mu);
-  g_timing = on != 0;
+  g_timing_mask.store(on ? ~0ull : 0ull);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_timing_enable_mask(unsigned long long kernel_mask) {
+  g_timing_mask.store(kernel_mask);
   return MOE_OK;
 }
 
