@@ -65,7 +65,8 @@ def get_shape(name):
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    """Samples SM clocks and throttle reasons with nvidia-smi every 20 ms while running;
+    only the samples taken inside the marked window count."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -74,14 +75,18 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []     # (host time the line arrived, line)
         self.thread = None
+        self.window = (0.0, float("inf"))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -91,7 +96,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def stop(self):
         if self.proc is None:
@@ -105,7 +110,9 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if not (self.window[0] <= t <= self.window[1]):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -254,6 +261,10 @@ def main():
     torch.cuda.synchronize()
     assert layer.device_error()[0] == B.MOE_OK
 
+    sampler = ClockSampler(local)   # nvidia-smi needs a moment to start
+    sampler.start()
+    time.sleep(0.3)
+
     # ---------------- per-kernel table: a separate pass with every launch bracketed by
     # CUDA events (the events cost ~2% of a step, so the timed region below brackets only
     # the dominant GEMM)
@@ -269,11 +280,9 @@ def main():
     dom = max(gemm_times, key=gemm_times.get) if gemm_times else None
 
     # ---------------- timed region (device-resident inputs)
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     launches0, _ = B.moe_launch_count()
     B.moe_timing_enable_only([dom] if dom else [])
+    t_load0 = time.perf_counter()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -290,7 +299,6 @@ def main():
         dist.barrier()
     B.moe_timing_enable(False)
     launches1, _ = B.moe_launch_count()
-    clocks = sampler.stop()
     dom_timed = B.moe_timing_collect()   # the dominant GEMM's launches inside the timed region
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     fwd_ms = [a.elapsed_time(b) for a, b in zip(starts, mids)]
@@ -364,6 +372,10 @@ def main():
     e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    t_load1 = time.perf_counter()
+    sampler.mark(t_load0, t_load1)   # clocks under load: the timed region and the e2e run
+    clocks = sampler.stop()
+    clocks["window"] = "timed region and end-to-end run"
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = job_throughput(step_flops, world, e2e_ms / args.steps * 1e-3) / 1e12
     assert layer.device_error()[0] == B.MOE_OK
