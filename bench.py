@@ -34,6 +34,30 @@ GEMM_FLOPS_RDI = {"gemm_gateup_swiglu": 4, "gemm_down": 2, "gemm_dA": 2, "gemm_b
                   "gemm_dx": 4, "gemm_dw_gateup": 4, "gemm_dw_down": 2}
 
 
+def movement_bytes(s):
+    """Algorithmic bytes per launch of the HBM-bound kernels (what each must read and
+    write at the minimum): permute (x rows in, sorted rows out, slot ids and weights),
+    combine (sorted rows in, token rows out, inverse permutation and weights) and the
+    backward's row preparation (dY and x rows in; dY_perm, its fp16 copy and the fp16
+    copy of x_perm out)."""
+    T, R, D = s.T, s.R, s.D
+    return {"gather_x": T * D * 2 + R * D * 2 + 8 * R,
+            "combine": R * D * 2 + 8 * R + T * D * 2,
+            "bwd_prep_rows": 2 * T * D * 2 + 3 * R * D * 2 + 4 * R}
+
+
+def direction_bytes(s):
+    """Minimum bytes each direction must move: forward X, all expert weights, Y;
+    backward X, dY, the weights, dX and the fp32 weight gradients."""
+    w = 3 * s.E * s.D * s.I
+    return {"fwd": 2 * s.T * s.D * 2 + w * 2, "bwd": 3 * s.T * s.D * 2 + w * 2 + w * 4}
+
+
+def pct(xs, q):
+    xs = sorted(xs)
+    return xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -381,6 +405,27 @@ def main():
     assert layer.device_error()[0] == B.MOE_OK
     assert torch.equal(out_y[(args.steps - 1) % 2].to(dev), layer.y)
 
+    # ---------------- the same step captured once as a CUDA graph and replayed
+    def graph_step():
+        layer.forward(inp["x"], inp["topk_ids"], inp["topk_w"], wg, wu, wd)
+        layer.backward(inp["dy"], wg, wu, wd)
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        graph_step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps
+    assert layer.device_error()[0] == B.MOE_OK
+
     # ---------------- roofline of the dominant kernel (largest share of the step)
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -394,6 +439,15 @@ def main():
             ent["tflops"] = tf
             ent["frac_of_sustained_peak"] = tf / peak
         kernels[k] = ent
+    hbm_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    for k, nbytes in movement_bytes(s).items():
+        if k in kernels:
+            gbs = nbytes / (kernels[k]["ms_per_launch"] * 1e-3) / 1e9
+            kernels[k]["gbs"] = gbs
+            kernels[k]["frac_of_hbm"] = gbs / hbm_gbs
+    db = direction_bytes(s)
+    roof_fwd = min(peak_tf, s.fwd_flops() / db["fwd"] * hbm_gbs * 1e9 / 1e12)
+    roof_bwd = min(peak_tf, s.bwd_flops() / db["bwd"] * hbm_gbs * 1e9 / 1e12)
     achieved = dom_ms = None
     if dom and dom in dom_timed:
         ms_d, n_d = dom_timed[dom]
@@ -425,7 +479,15 @@ def main():
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         "fwd_frac_of_peak": fwd_tflops / peak_tf, "bwd_frac_of_peak": bwd_tflops / peak_tf,
         "peak_bf16_tflops": peak_tf, "peak_source": peak_src,
+        "fwd_frac_of_roof": fwd_tflops / roof_fwd, "bwd_frac_of_roof": bwd_tflops / roof_bwd,
+        "roof_tflops": {"fwd": roof_fwd, "bwd": roof_bwd,
+                        "note": "min(dense bf16 peak, algorithmic FLOP/byte x measured HBM GB/s)"},
         "fwd_ms_median": statistics.median(fwd_ms), "bwd_ms_median": statistics.median(bwd_ms),
+        "fwd_ms_p10_p90": [pct(fwd_ms, 0.1), pct(fwd_ms, 0.9)],
+        "bwd_ms_p10_p90": [pct(bwd_ms, 0.1), pct(bwd_ms, 0.9)],
+        "graph": {"ms_per_step": graph_ms,
+                  "value": job_throughput(step_flops, world, graph_ms * 1e-3) / 1e12,
+                  "note": "the same step captured once as a CUDA graph and replayed"},
         "step_ms_median": statistics.median(step_ms),
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
                      "ms_per_launch": dom_ms,
