@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef uint16_t moe_bf16_t;
 
@@ -170,6 +170,51 @@ int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x, const moe_bf16
                        const moe_bf16_t* w_down, int T, int K, int E, int D, int I, int align,
                        moe_bf16_t* dx_perm, float* dw_gate, float* dw_up, float* dw_down,
                        void* workspace, void* stream);
+
+/* ---- router step ------------------------------------------------------------
+ * The pages have the forward's final combine apply the router weights ("LigerMoE
+ * design / Forward pass"); how the weights arise is fixed by the workloads the layer
+ * is measured on.  These calls produce the routing that moe_route_permute consumes and
+ * the gradients that flow back into the router. */
+typedef enum {
+  MOE_ROUTER_SOFTMAX_TOPK = 0,  /* softmax over all E logits, the K largest, renormalised */
+  MOE_ROUTER_SIGMOID_TOP1 = 1   /* the largest logit's expert, weight sigmoid(logit); K = 1 */
+} moe_router_t;
+
+/*
+ * For every token t: the K experts of largest logits[t,:] (equal logits: the lower
+ * expert index first; slot k = 0 holds the largest), and their weights:
+ *   SOFTMAX_TOPK  topk_w[t,k] = softmax(logits[t,:])_{e_k} / sum_j softmax(logits[t,:])_{e_j}
+ *                 (= the softmax over the K chosen logits), fp32
+ *   SIGMOID_TOP1  topk_w[t,0] = 1 / (1 + exp(-logits[t,e_0]))
+ *   logits [T,E] fp32 -> topk_ids [T,K] int32, topk_w [T,K] fp32, all device.
+ * Constraints: T >= 0, 1 <= K <= 32, K <= E <= 1024, SIGMOID_TOP1 needs K == 1.
+ * The expert choice is made on the fp32 logits exactly (bit-reproducible).
+ */
+int moe_router_topk(const float* logits, int T, int E, int K, int router, int32_t* topk_ids,
+                    float* topk_w, void* stream);
+
+/*
+ * Router-weight gradient of L = sum(Y * dY), Y[t] = sum_k topk_w[t,k] f_{e_k}(x[t]):
+ *   d_topk_w[t,k] = sum_d dy[t,d] * y_perm[inv_perm[t*K+k], d]     (fp32 sum)
+ * where y_perm is moe_expert_mlp_fwd's output (the unweighted expert outputs, in
+ * sorted order) and inv_perm moe_route_permute's.  dy [T,D] bf16, y_perm [cap,D] bf16,
+ * inv_perm [T*K] int32 -> d_topk_w [T,K] fp32, all device.  D % 8 == 0.
+ */
+int moe_router_weight_grad(const moe_bf16_t* dy, const moe_bf16_t* y_perm,
+                           const int32_t* inv_perm, int T, int K, int D, float* d_topk_w,
+                           void* stream);
+
+/*
+ * Logit gradient through the router weights (the expert choice is piecewise constant in
+ * the logits and contributes nothing):
+ *   SOFTMAX_TOPK  d_logits[t,e_k] = w_k (dw_k - sum_j w_j dw_j), zero for unchosen experts
+ *   SIGMOID_TOP1  d_logits[t,e_0] = dw_0 w_0 (1 - w_0), zero elsewhere
+ *   topk_ids, topk_w from moe_router_topk; d_topk_w [T,K] fp32 -> d_logits [T,E] fp32
+ *   (fully overwritten), all device.  Constraints as moe_router_topk.
+ */
+int moe_router_backward(const int32_t* topk_ids, const float* topk_w, const float* d_topk_w,
+                        int T, int E, int K, int router, float* d_logits, void* stream);
 
 /*
  * moe_route_permute without a workspace, for callers that cannot allocate device

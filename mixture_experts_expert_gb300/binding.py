@@ -55,6 +55,9 @@ _SIGS = {
     "moe_kernel_name": (ctypes.c_char_p, [_I]),
     "moe_launch_count": (ctypes.c_longlong, [ctypes.POINTER(ctypes.c_longlong)]),
     "moe_timing_enable": (_I, [_I]),
+    "moe_router_topk": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_router_weight_grad": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_router_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_timing_enable_mask": (_I, [ctypes.c_ulonglong]),
     "moe_timing_collect": (_I, [ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(ctypes.c_longlong)]),
@@ -193,6 +196,34 @@ def moe_expert_mlp_bwd(dy, x, x_perm, perm_src, w_perm, offsets, counts, w_gate,
         _ptr(dx_perm, bf, "dx_perm"), _ptr(dw_gate, f32, "dw_gate"), _ptr(dw_up, f32, "dw_up"),
         _ptr(dw_down, f32, "dw_down"), _ptr(workspace, name="workspace"), _stream(stream))
     _check("moe_expert_mlp_bwd", st)
+
+
+ROUTERS = {"softmax": 0, "sigmoid_top1": 1}
+
+
+def moe_router_topk(logits, T, E, K, router, topk_ids, topk_w, stream=None):
+    st = lib().moe_router_topk(
+        _ptr(logits, torch.float32, "logits", T == 0), T, E, K, ROUTERS[router],
+        _ptr(topk_ids, torch.int32, "topk_ids", T == 0),
+        _ptr(topk_w, torch.float32, "topk_w", T == 0), _stream(stream))
+    _check("moe_router_topk", st)
+
+
+def moe_router_weight_grad(dy, y_perm, inv_perm, T, K, D, d_topk_w, stream=None):
+    st = lib().moe_router_weight_grad(
+        _ptr(dy, torch.bfloat16, "dy", T == 0), _ptr(y_perm, torch.bfloat16, "y_perm", T == 0),
+        _ptr(inv_perm, torch.int32, "inv_perm", T == 0), T, K, D,
+        _ptr(d_topk_w, torch.float32, "d_topk_w", T == 0), _stream(stream))
+    _check("moe_router_weight_grad", st)
+
+
+def moe_router_backward(topk_ids, topk_w, d_topk_w, T, E, K, router, d_logits, stream=None):
+    st = lib().moe_router_backward(
+        _ptr(topk_ids, torch.int32, "topk_ids", T == 0),
+        _ptr(topk_w, torch.float32, "topk_w", T == 0),
+        _ptr(d_topk_w, torch.float32, "d_topk_w", T == 0), T, E, K, ROUTERS[router],
+        _ptr(d_logits, torch.float32, "d_logits", T == 0), _stream(stream))
+    _check("moe_router_backward", st)
 
 
 def moe_get_device_error(workspace, stream=None):

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libmoe_gb300.so")
 
-SOURCES = ["moe_api.cu", "route.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_dw.cu"]
+SOURCES = ["moe_api.cu", "route.cu", "router.cu", "gemm_fwd.cu", "gemm_bwd.cu", "gemm_dw.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -33,6 +33,9 @@ enum KernelId : int {
   kKDwPrep,
   kKGemmDwGU,
   kKGemmDwD,
+  kKRouterTopk,
+  kKRouterWGrad,
+  kKRouterBwd,
   kNumKernelIds
 };
 
@@ -111,5 +114,14 @@ cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float*
                            float* dw_up, float* dw_down, int D, int I, cudaStream_t s);
 
 int route_num_chunks(int R);
+
+// Router step (router: 0 = softmax top-K renormalised, 1 = sigmoid of the top-1 logit).
+cudaError_t launch_router_topk(const float* logits, int T, int E, int K, int router, int32_t* ids,
+                               float* w, cudaStream_t s);
+cudaError_t launch_router_backward(const int32_t* ids, const float* w, const float* dw, int T,
+                                   int E, int K, int router, float* dz, cudaStream_t s);
+cudaError_t launch_router_weight_grad(const uint16_t* dy, const uint16_t* y_perm,
+                                      const int32_t* inv, int T, int K, int D, float* dw,
+                                      cudaStream_t s);
 
 }  // namespace moe

@@ -16,7 +16,8 @@ namespace moe {
 static const char* const kKernelNames[kNumKernelIds] = {
     "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
     "gemm_down",   "combine",    "bwd_prep_rows", "gemm_dA",    "gemm_bwd_gateup",
-    "gemm_dx",     "dw_prep",    "gemm_dw_gateup", "gemm_dw_down"};
+    "gemm_dx",     "dw_prep",    "gemm_dw_gateup", "gemm_dw_down", "router_topk",
+    "router_weight_grad", "router_backward"};
 
 const char* kernel_name(int id) {
   return (id >= 0 && id < kNumKernelIds) ? kKernelNames[id] : nullptr;
@@ -507,6 +508,47 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
     e = launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, f->num_sms, s);
   }
   return to_status(e);
+}
+
+static bool router_args_ok(int T, int E, int K, int router) {
+  if (T < 0 || K < 1 || K > 32 || E < K || E > kMaxExperts) return false;
+  if (router != MOE_ROUTER_SOFTMAX_TOPK && router != MOE_ROUTER_SIGMOID_TOP1) return false;
+  if (router == MOE_ROUTER_SIGMOID_TOP1 && K != 1) return false;
+  return static_cast<long long>(T) * (E > K ? E : K) < (1ll << 31);
+}
+
+MOE_EXPORT int moe_router_topk(const float* logits, int T, int E, int K, int router,
+                               int32_t* topk_ids, float* topk_w, void* stream) {
+  if (!router_args_ok(T, E, K, router)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_ids || !topk_w)) return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  return to_status(launch_router_topk(logits, T, E, K, router, topk_ids, topk_w,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_router_weight_grad(const moe_bf16_t* dy, const moe_bf16_t* y_perm,
+                                      const int32_t* inv_perm, int T, int K, int D,
+                                      float* d_topk_w, void* stream) {
+  if (T < 0 || K < 1 || K > 32 || D <= 0 || D % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * K >= (1ll << 31)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!dy || !y_perm || !inv_perm || !d_topk_w)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!aligned16(dy) || !aligned16(y_perm))) return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  return to_status(launch_router_weight_grad(dy, y_perm, inv_perm, T, K, D, d_topk_w,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+MOE_EXPORT int moe_router_backward(const int32_t* topk_ids, const float* topk_w,
+                                   const float* d_topk_w, int T, int E, int K, int router,
+                                   float* d_logits, void* stream) {
+  if (!router_args_ok(T, E, K, router)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !topk_w || !d_topk_w || !d_logits)) return MOE_ERR_INVALID_ARG;
+  int st = check_device();
+  if (st != MOE_OK) return st;
+  return to_status(launch_router_backward(topk_ids, topk_w, d_topk_w, T, E, K, router, d_logits,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 MOE_EXPORT int moe_get_device_error(void* workspace, int* code, int* detail, void* stream) {
