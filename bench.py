@@ -426,6 +426,26 @@ def main():
     graph_ms = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps
     assert layer.device_error()[0] == B.MOE_OK
 
+    # ---------------- the router step (not part of the expert-MLP metric): routing from
+    # the workload's logits, and the logit gradient after the backward
+    logits = inp["logits"].to(dev)
+
+    def router_step():
+        layer.route(logits, s.router)
+        layer.router_backward(inp["dy"])
+
+    router_step()
+    torch.cuda.synchronize()
+    B.moe_timing_collect()
+    B.moe_timing_enable_only(["router_topk", "router_weight_grad", "router_backward"])
+    for _ in range(args.steps):
+        router_step()
+    torch.cuda.synchronize()
+    B.moe_timing_enable(False)
+    router_ms = {k: v[0] / v[1] for k, v in B.moe_timing_collect().items()}
+    # the routing the kernel chose is the routing the inputs were generated with
+    routed_same = bool(torch.equal(layer.topk_ids, inp["topk_ids"]))
+
     # ---------------- roofline of the dominant kernel (largest share of the step)
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -501,6 +521,10 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,
+        "router": {"ms_per_launch": router_ms, "same_routing_as_inputs": routed_same,
+                   "weight_grad_gbs": (s.R * s.D * 2 + s.T * s.D * 2) /
+                                      (router_ms.get("router_weight_grad", float("nan")) * 1e-3) / 1e9,
+                   "note": "router step, outside the expert-MLP metric"},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s)

@@ -15,6 +15,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "internal.h"
 
 namespace moe {
@@ -31,7 +33,7 @@ __device__ __forceinline__ bool better(float v, int i, float w, int j) {
 // Softmax over all E logits, top-K, renormalised == softmax over the K chosen logits
 // (the full normaliser cancels); the choice is made on the logits themselves, which
 // order exactly as the probabilities do.
-template <int kRouter>
+template <int kRouter, int kPerLane>
 __global__ void __launch_bounds__(32 * kRouterWarps) k_router_topk(
     const float* __restrict__ logits, int T, int E, int K, int32_t* __restrict__ ids,
     float* __restrict__ w) {
@@ -39,22 +41,22 @@ __global__ void __launch_bounds__(32 * kRouterWarps) k_router_topk(
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
   const float* z = logits + static_cast<size_t>(t) * E;
-  float v[kMaxPerLane];
+  float v[kPerLane];   // lane holds logits lane, lane + 32, ... (E <= 32 * kPerLane)
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) {
+  for (int j = 0; j < kPerLane; ++j) {
     const int e = lane + 32 * j;
     v[j] = e < E ? __ldg(z + e) : -INFINITY;
   }
-  bool taken[kMaxPerLane];
+  bool taken[kPerLane];
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) taken[j] = lane + 32 * j >= E;
+  for (int j = 0; j < kPerLane; ++j) taken[j] = lane + 32 * j >= E;
   float my_val = 0.f;   // lane k keeps the k-th chosen logit and expert
   int my_idx = 0;
   for (int k = 0; k < K; ++k) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
+    for (int j = 0; j < kPerLane; ++j) {
       const int e = lane + 32 * j;
       if (!taken[j] && better(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
     }
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(32 * kRouterWarps) k_router_topk(
     }
     if ((bi & 31) == lane) {
 #pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j)
+      for (int j = 0; j < kPerLane; ++j)
         if (lane + 32 * j == bi) taken[j] = true;
     }
     if (lane == k) { my_val = bv; my_idx = bi; }
@@ -116,53 +118,43 @@ __global__ void __launch_bounds__(32 * kRouterWarps) k_router_backward(
   if (lane < K) row[__ldg(ids + o)] = g;
 }
 
-// d_topk_w[t,k] = <dy[t], y_perm[inv[t*K+k]]>: the token's dY row against each of its K
-// sorted expert-output rows, 16-byte loads, fp32 sums.
+// d_topk_w[t,k] = <dy[t], y_perm[inv[t*K+k]]>: one warp per routed slot streams its
+// sorted expert-output row against the token's dY row (read K times, from cache),
+// 16-byte loads, two vectors in flight per lane, fp32 sums.
 __global__ void __launch_bounds__(32 * kRouterWarps) k_router_weight_grad(
     const uint16_t* __restrict__ dy, const uint16_t* __restrict__ y_perm,
     const int32_t* __restrict__ inv, int T, int K, int D, float* __restrict__ dw) {
-  const int t = blockIdx.x * kRouterWarps + (threadIdx.x >> 5);
+  const long long j = static_cast<long long>(blockIdx.x) * kRouterWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  if (j >= static_cast<long long>(T) * K) return;
+  const int t = static_cast<int>(j / K);
   const int nvec = D >> 3;
   const uint4* d = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(t) * D);
-  const int my_row = lane < K ? __ldg(inv + static_cast<size_t>(t) * K + lane) : 0;
-  int rows[32];   // the K sorted rows, in every lane (taken while the whole warp is converged)
+  const uint4* y = reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(__ldg(inv + j)) * D);
+  float acc = 0.f;
+  for (int vi = lane; vi < nvec; vi += 64) {
+    uint4 dq[2], yq[2];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) rows[k] = __shfl_sync(0xffffffffu, my_row, k);
-  float acc[32];
-#pragma unroll
-  for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-  for (int vi = lane; vi < nvec; vi += 32) {
-    const uint4 dq = __ldg(d + vi);
-    const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&dq);
-    float df[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = __bfloat1622float2(dh[i]);
-      df[2 * i] = f.x;
-      df[2 * i + 1] = f.y;
+    for (int h = 0; h < 2; ++h) {
+      const int v = vi + 32 * h;
+      dq[h] = v < nvec ? __ldg(d + v) : make_uint4(0, 0, 0, 0);
+      yq[h] = v < nvec ? __ldg(y + v) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      if (k < K) {
-        const uint4 yq =
-            __ldg(reinterpret_cast<const uint4*>(y_perm + static_cast<size_t>(rows[k]) * D) + vi);
-        const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yq);
+    for (int h = 0; h < 2; ++h) {
+      const __nv_bfloat162* dh = reinterpret_cast<const __nv_bfloat162*>(&dq[h]);
+      const __nv_bfloat162* yh = reinterpret_cast<const __nv_bfloat162*>(&yq[h]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(yh[i]);
-          acc[k] += df[2 * i] * f.x + df[2 * i + 1] * f.y;
-        }
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = __bfloat1622float2(dh[i]);
+        const float2 b = __bfloat1622float2(yh[i]);
+        acc += a.x * b.x + a.y * b.y;
       }
     }
   }
-  for (int k = 0; k < K; ++k) {
-    float s = acc[k];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) dw[static_cast<size_t>(t) * K + k] = s;
-  }
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) dw[j] = acc;
 }
 
 }  // namespace
@@ -172,10 +164,18 @@ cudaError_t launch_router_topk(const float* logits, int T, int E, int K, int rou
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kRouterWarps - 1) / kRouterWarps;
   LaunchScope ls(kKRouterTopk, s);
-  if (router == 0)
-    k_router_topk<0><<<blocks, 32 * kRouterWarps, 0, s>>>(logits, T, E, K, ids, w);
-  else
-    k_router_topk<1><<<blocks, 32 * kRouterWarps, 0, s>>>(logits, T, E, K, ids, w);
+  // the fewest logits per lane that hold a row
+  auto go = [&](auto per_lane) {
+    constexpr int P = decltype(per_lane)::value;
+    if (router == 0) k_router_topk<0, P><<<blocks, 32 * kRouterWarps, 0, s>>>(logits, T, E, K, ids, w);
+    else k_router_topk<1, P><<<blocks, 32 * kRouterWarps, 0, s>>>(logits, T, E, K, ids, w);
+  };
+  if (E <= 32) go(std::integral_constant<int, 1>());
+  else if (E <= 64) go(std::integral_constant<int, 2>());
+  else if (E <= 128) go(std::integral_constant<int, 4>());
+  else if (E <= 256) go(std::integral_constant<int, 8>());
+  else if (E <= 512) go(std::integral_constant<int, 16>());
+  else go(std::integral_constant<int, kMaxPerLane>());
   return cudaGetLastError();
 }
 
@@ -195,7 +195,8 @@ cudaError_t launch_router_weight_grad(const uint16_t* dy, const uint16_t* y_perm
                                       const int32_t* inv, int T, int K, int D, float* dw,
                                       cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const int blocks = (T + kRouterWarps - 1) / kRouterWarps;
+  const long long slots = static_cast<long long>(T) * K;
+  const int blocks = static_cast<int>((slots + kRouterWarps - 1) / kRouterWarps);
   LaunchScope ls(kKRouterWGrad, s);
   k_router_weight_grad<<<blocks, 32 * kRouterWarps, 0, s>>>(dy, y_perm, inv, T, K, D, dw);
   return cudaGetLastError();

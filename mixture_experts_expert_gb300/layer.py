@@ -2,6 +2,8 @@
 C ABI needs (allocated once with torch, reused by every call) and strings the
 entry points together.
 
+Router (optional): moe_router_topk (logits -> topk_ids, topk_w); after the backward,
+moe_router_weight_grad + moe_router_backward (-> d_logits).
 Forward:  moe_route_permute -> moe_expert_mlp_fwd -> moe_combine(topk_w)
 Backward: moe_expert_mlp_bwd -> moe_combine(NULL)   (reduces routed dX to tokens)
 
@@ -71,6 +73,29 @@ class MoEExpertMLP:
                              self.dw_gate, self.dw_up, self.dw_down, self.workspace, stream)
         B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, self.dx, stream)
         return self.dx, self.dw_gate, self.dw_up, self.dw_down
+
+    def route(self, logits, router="softmax", stream=None):
+        """(topk_ids [T,K] int32, topk_w [T,K] fp32) from router logits [T,E] fp32."""
+        T, K, E = self.T, self.K, self.E
+        if not hasattr(self, "topk_ids"):
+            self.topk_ids = torch.empty(T, K, dtype=torch.int32, device=self.device)
+            self.topk_w = torch.empty(T, K, dtype=torch.float32, device=self.device)
+        B.moe_router_topk(logits, T, E, K, router, self.topk_ids, self.topk_w, stream)
+        self._router = router
+        return self.topk_ids, self.topk_w
+
+    def router_backward(self, dy, stream=None):
+        """d_logits [T,E] fp32 for the routing of the last route() + forward(): the
+        router-weight gradient <dY[t], f_e(x[t])> from the forward's expert outputs,
+        then through the router weights to the logits."""
+        T, K, E, D = self.T, self.K, self.E, self.D
+        if not hasattr(self, "d_topk_w"):
+            self.d_topk_w = torch.empty(T, K, dtype=torch.float32, device=self.device)
+            self.d_logits = torch.empty(T, E, dtype=torch.float32, device=self.device)
+        B.moe_router_weight_grad(dy, self.y_perm, self.inv_perm, T, K, D, self.d_topk_w, stream)
+        B.moe_router_backward(self.topk_ids, self.topk_w, self.d_topk_w, T, E, K, self._router,
+                              self.d_logits, stream)
+        return self.d_logits
 
     def _counts(self):
         return self.counts if self.skip_padding else None
