@@ -214,8 +214,10 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
   for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < rows; s += wpg) {
     const int j = __ldg(perm_src + s);
     uint4* d = reinterpret_cast<uint4*>(dst + static_cast<size_t>(s) * D);
+    // the sorted rows are written once and not read again here: streaming stores keep
+    // them from evicting the token rows, which K slots each read from cache
     if (j < 0) {
-      for (int v = lane; v < nvec; v += 32) d[v] = make_uint4(0, 0, 0, 0);
+      for (int v = lane; v < nvec; v += 32) __stcs(d + v, make_uint4(0, 0, 0, 0));
       continue;
     }
     const uint4* sp = reinterpret_cast<const uint4*>(src + static_cast<size_t>(j / K) * D);
@@ -228,12 +230,12 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint16_t* __restrict_
         q0 = scale_bf16x8(q0, sc); q1 = scale_bf16x8(q1, sc);
         q2 = scale_bf16x8(q2, sc); q3 = scale_bf16x8(q3, sc);
       }
-      d[v] = q0; d[v + 32] = q1; d[v + 64] = q2; d[v + 96] = q3;
+      __stcs(d + v, q0); __stcs(d + v + 32, q1); __stcs(d + v + 64, q2); __stcs(d + v + 96, q3);
     }
     for (; v < nvec; v += 32) {
       uint4 q = __ldg(sp + v);
       if (SCALE) q = scale_bf16x8(q, sc);
-      d[v] = q;
+      __stcs(d + v, q);
     }
   }
 }
@@ -281,9 +283,9 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     if (j < 0) {
       const uint4 z = make_uint4(0, 0, 0, 0);
       for (int v = lane; v < nvec; v += 32) {
-        dp[v] = z;
-        d16[v] = z;
-        x16p[v] = z;
+        __stcs(dp + v, z);
+        __stcs(d16 + v, z);
+        __stcs(x16p + v, z);
       }
       continue;
     }
@@ -294,9 +296,9 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     for (int v = lane; v < nvec; v += 32) {
       const uint4 q = __ldg(sp + v);
       const uint4 xq = __ldg(xp + v);
-      dp[v] = q;
-      d16[v] = bf16x8_to_f16x8(q);
-      x16p[v] = bf16x8_to_f16x8(xq);
+      __stcs(dp + v, q);            // streaming stores: the dY / x rows stay cached
+      __stcs(d16 + v, bf16x8_to_f16x8(q));
+      __stcs(x16p + v, bf16x8_to_f16x8(xq));
     }
   }
 }
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ sr
         const uint4* rp = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * D);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          q[h][u] = (act[h] && k < K) ? __ldg(rp + vv[h]) : make_uint4(0, 0, 0, 0);
+          q[h][u] = (act[h] && k < K) ? __ldcs(rp + vv[h]) : make_uint4(0, 0, 0, 0);   // read once
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
