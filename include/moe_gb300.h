@@ -245,7 +245,9 @@ int moe_route_permute_noalloc(const int32_t* topk_ids, const float* topk_w,
 /*
  * Reads and clears the device error word of `workspace` (synchronises `stream`).
  * *code receives MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT; *detail the
- * raw device code (which role timed out).  For tests and debugging.
+ * raw device code (which role timed out).  After an error it also zeroes the rest of the
+ * workspace header (counters a kernel that gave up may leave set): call it, or
+ * moe_workspace_init, before reusing a workspace after an error.  For tests and debugging.
  */
 int moe_get_device_error(void* workspace, int* code, int* detail, void* stream);
 

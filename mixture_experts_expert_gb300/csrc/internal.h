@@ -15,6 +15,7 @@ enum DevErr : int {
   kDevTimeoutProducer = 2,  // TMA producer gave up waiting on a free stage
   kDevTimeoutMma = 3,       // MMA issuer gave up waiting on data or TMEM
   kDevTimeoutEpilogue = 4,  // epilogue gave up waiting on an accumulator
+  kDevTimeoutRoute = 6,     // the fused routing kernel gave up at a grid barrier
 };
 
 // Identifiers of every kernel the library launches (for launch counting and timing).
@@ -36,6 +37,7 @@ enum KernelId : int {
   kKRouterTopk,
   kKRouterWGrad,
   kKRouterBwd,
+  kKRouteFused,
   kNumKernelIds
 };
 
@@ -93,7 +95,7 @@ cudaError_t launch_gemm_kind(const GemmParams& p, int max_tiles, int num_sms, cu
 cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, int T, int K,
                          int E, int D, int align, int cap, int32_t* counts, int32_t* offsets,
                          int32_t* perm_src, int32_t* inv_perm, float* w_perm, uint16_t* x_perm,
-                         int32_t* chunk_counts, int* err, cudaStream_t s);
+                         int32_t* chunk_counts, int* err, unsigned* sync, cudaStream_t s);
 
 cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, const float* w_perm,
                                const int32_t* offsets, int E, int K, int D, int cap,

@@ -17,7 +17,7 @@ static const char* const kKernelNames[kNumKernelIds] = {
     "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
     "gemm_down",   "combine",    "bwd_prep_rows", "gemm_dA",    "gemm_bwd_gateup",
     "gemm_dx",     "dw_prep",    "gemm_dw_gateup", "gemm_dw_down", "router_topk",
-    "router_weight_grad", "router_backward"};
+    "router_weight_grad", "router_backward", "route_permute"};
 
 const char* kernel_name(int id) {
   return (id >= 0 && id < kNumKernelIds) ? kKernelNames[id] : nullptr;
@@ -261,6 +261,10 @@ MOE_EXPORT const char* moe_status_string(int status) {
   }
 }
 
+// Workspace header: [0] device error word; at kRouteSyncOffset the fused routing kernel's
+// grid-barrier counters {arrivals, exits} (zero between launches).
+constexpr size_t kRouteSyncOffset = 512;
+
 MOE_EXPORT size_t moe_capacity(int T, int K, int E, int align) {
   if (!basic_sizes_ok(T, K, E, align)) return 0;
   return capacity_of(T, K, E, align);
@@ -295,7 +299,9 @@ MOE_EXPORT int moe_route_permute(const int32_t* topk_ids, const float* topk_w,
   return to_status(launch_route(topk_ids, topk_w, x, T, K, E, D, align, cap, counts, offsets,
                                 perm_src, inv_perm, w_perm, x_perm,
                                 reinterpret_cast<int32_t*>(ws + L.chunk_counts),
-                                reinterpret_cast<int*>(ws), static_cast<cudaStream_t>(stream)));
+                                reinterpret_cast<int*>(ws),
+                                reinterpret_cast<unsigned*>(ws + kRouteSyncOffset),
+                                static_cast<cudaStream_t>(stream)));
 }
 
 MOE_EXPORT int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm,
@@ -563,7 +569,8 @@ MOE_EXPORT int moe_get_device_error(void* workspace, int* code, int* detail, voi
   else if (raw == kDevBadExpertId) *code = MOE_ERR_BAD_INDEX;
   else *code = MOE_ERR_DEVICE_TIMEOUT;
   if (raw != 0) {
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // clears the word and the header's barrier counters a kernel that gave up may leave set
+    if (cudaMemsetAsync(workspace, 0, 1024, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
