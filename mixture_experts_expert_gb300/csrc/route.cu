@@ -147,11 +147,10 @@ __global__ void __launch_bounds__(kRouteWarps * 32) k_route_scatter(
 // ------------------------------------------------------------------ fused routing
 // The routing phases in one cooperative launch (every block resident), separated by
 // grid barriers: (A) padding marks and per-chunk expert histograms, (B) per-expert scan
-// over the chunks, (C) padded offsets and the stable scatter, and optionally (D) the
-// gather of the token rows into x_perm (zero rows on padding).  One launch instead of
-// three saves their launch gaps and tails.  (D) is left to the separate gather kernel:
-// inside this launch it ran slower (measured 107 us for all four phases against 24.5 us
-// for (A)-(C) plus 60 us for the gather kernel).
+// over the chunks, (C) padded offsets and the stable scatter.  One launch instead of
+// three saves their launch gaps and tails.  The gather of the token rows stays a
+// separate kernel: folded into this launch as a fourth phase it ran slower (measured
+// 107 us for the four phases against 24.5 us for these three plus 60 us for the gather).
 
 // Waits until `target` blocks have arrived at *ctr (a counter that only grows during the
 // launch).  Bounded: after kWaitLimitNs it records a timeout and returns false.
@@ -182,12 +181,10 @@ __device__ __forceinline__ bool grid_barrier(unsigned* ctr, unsigned target, int
 }
 
 __global__ void __launch_bounds__(kRouteWarps * 32) k_route_fused(
-    const int32_t* __restrict__ ids, const float* __restrict__ w, const uint16_t* __restrict__ x,
-    int R, int K, int E, int D, int align, int nchunks, int cap,
-    int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int R, int E, int align,
+    int nchunks, int cap, int32_t* __restrict__ chunk_counts, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
-    int32_t* __restrict__ inv_perm, float* __restrict__ w_perm, uint16_t* __restrict__ x_perm,
-    unsigned* sync, int* err) {
+    int32_t* __restrict__ inv_perm, float* __restrict__ w_perm, unsigned* sync, int* err) {
   extern __shared__ int sh[];          // per warp: E ints (histogram, then running rows)
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_warp[32];
@@ -289,28 +286,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32) k_route_fused(
     }
     __syncwarp();
   }
-  if (x != nullptr) {
-    if (!grid_barrier(sync, 3 * nb, err, &s_ok)) return;
-    // (D) the token rows, one warp per sorted row; streaming stores keep x in cache
-    const int rows = s_off[E];
-    const int nvec = D >> 3;
-    for (int sr = gw; sr < rows; sr += nw) {
-      const int j = __ldcg(perm_src + sr);
-      uint4* d = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(sr) * D);
-      if (j < 0) {
-        for (int v = lane; v < nvec; v += 32) __stcs(d + v, make_uint4(0, 0, 0, 0));
-        continue;
-      }
-      const uint4* sp = reinterpret_cast<const uint4*>(x + static_cast<size_t>(j / K) * D);
-      int v = lane;
-      for (; v + 96 < nvec; v += 128) {
-        const uint4 q0 = __ldg(sp + v), q1 = __ldg(sp + v + 32), q2 = __ldg(sp + v + 64),
-                    q3 = __ldg(sp + v + 96);
-        __stcs(d + v, q0); __stcs(d + v + 32, q1); __stcs(d + v + 64, q2); __stcs(d + v + 96, q3);
-      }
-      for (; v < nvec; v += 32) __stcs(d + v, __ldg(sp + v));
-    }
-  }
   // the last block out resets the barrier counter for the next launch
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -357,9 +332,8 @@ cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, 
     cudaError_t e;
     {
       LaunchScope ls(kKRouteFused, s);
-      e = cudaLaunchKernelEx(&cfg, k_route_fused, ids, w, static_cast<const uint16_t*>(nullptr), R,
-                             K, E, D, align, nch, cap, chunk_counts, counts, offsets, perm_src,
-                             inv_perm, w_perm, x_perm, sync, err);
+      e = cudaLaunchKernelEx(&cfg, k_route_fused, ids, w, R, E, align, nch, cap, chunk_counts,
+                             counts, offsets, perm_src, inv_perm, w_perm, sync, err);
     }
     if (e == cudaSuccess && x != nullptr)
       e = launch_gather_rows(x, perm_src, nullptr, offsets, E, K, D, cap, x_perm, kKGatherX, s);
