@@ -657,7 +657,13 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
         if (lane == 0) mbar_arrive(&bars->xfull[pi]);
         xph ^= 1u;
       }
-      return true;
+      // the staging buffer goes back to this warp's store ring with the next tile: the gate
+      // warp must have read the last chunk out of it first
+      int ok = 1;
+      if (lane == 0)
+        ok = mbar_wait(&bars->xempty[pi], xph ^ 1u, abort, p.err, kDevTimeoutEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      return ok != 0;
     }
     // gate warp: act columns f0 .. f0+31
     const int f0 = ti.n0 + 64 * rank + 32 * pi;

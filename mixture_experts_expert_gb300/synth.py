@@ -75,6 +75,9 @@ SKEWED = MoEShape("skewed_zipf1.2", T=16384, D=2048, I=768, E=128, K=8, w_std=0.
 # A steeper profile of the same family (s = 1.4) that leaves 15 experts without a token.
 SKEWED_STEEP = MoEShape("skewed_zipf1.4", T=16384, D=2048, I=768, E=128, K=8, w_std=0.02,
                         zipf_s=1.4)
+# The Zipf stress at the Llama-4-Scout shape (few, large experts; top-1 sigmoid router).
+SCOUT_SKEWED = MoEShape("llama4_scout_zipf1.2", T=8192, D=5120, I=8192, E=16, K=1,
+                        w_std=0.01, router="sigmoid_top1", zipf_s=1.2)
 
 
 def sweep_shape(T: int) -> MoEShape:
@@ -82,7 +85,8 @@ def sweep_shape(T: int) -> MoEShape:
     return dataclasses.replace(QWEN3_30B_A3B, name=f"qwen3_30b_a3b_T{T}", T=T)
 
 
-SHAPES = {s.name: s for s in (TINY, QWEN3_30B_A3B, LLAMA4_SCOUT, SKEWED, SKEWED_STEEP)}
+SHAPES = {s.name: s for s in (TINY, QWEN3_30B_A3B, LLAMA4_SCOUT, SKEWED, SKEWED_STEEP,
+                               SCOUT_SKEWED)}
 
 
 def route_from_logits(logits: torch.Tensor, K: int, router: str):

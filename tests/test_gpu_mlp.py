@@ -175,8 +175,9 @@ def _sample_experts(counts, rng):
 
 
 @pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.sweep_shape(1024),
-                                   synth.sweep_shape(2048), synth.SKEWED, synth.SKEWED_STEEP,
-                                   synth.LLAMA4_SCOUT], ids=lambda s: s.name)
+                                   synth.sweep_shape(2048), synth.sweep_shape(32768),
+                                   synth.sweep_shape(65536), synth.SKEWED, synth.SKEWED_STEEP,
+                                   synth.LLAMA4_SCOUT, synth.SCOUT_SKEWED], ids=lambda s: s.name)
 def test_full_size_workloads_sampled(shape):
     s = shape
     inp_dev = synth.make_inputs(s, device=DEV)
