@@ -36,9 +36,9 @@
 // The weight-gradient GEMMs sum over up to thousands of token rows, so their operands
 // are fp16 (10-bit mantissa; x and dY convert exactly) rather than bf16: the rounding of
 // the intermediates (dG, dU, w*act) is what bounds dW's absolute error.  dW tiles cover
-// at most kDwChunkRows token rows; an expert with more rows is split across tiles whose
-// fp32 results are TMA reduce-added into a zeroed dW, and its rows run twice (values,
-// then residuals) so that its error does not grow with the row count.
+// at most kDwChunkRows token rows; an expert with more rows is split into equal chunks on
+// tiles whose fp32 results are TMA reduce-added into a zeroed dW, and its rows run twice
+// (values, then residuals) so that its error does not grow with the row count.
 #pragma once
 
 #include "common.cuh"
@@ -231,7 +231,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, cons
     const int j = g - first;
     const int beg = __ldg(p.offsets + ti.e);
     const int end = __ldg(p.offsets + ti.e + 1);
-    ti.row0 = beg + j * kDwChunkRows;
+    // nch equal chunks (rounded up to 64 rows), so no chunk is a sliver
+    const int per = ((end - beg + nch - 1) / nch + kBK - 1) / kBK * kBK;
+    ti.row0 = beg + j * per;
     // K runs over the chunk's rows up to the expert's last real row (with counts) rounded
     // up to 64: the padding rows after it are zero in every operand
     int last = end;
@@ -240,7 +242,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, cons
       last = real < end ? real : end;
     }
     int rows = last - ti.row0;
-    rows = rows < kDwChunkRows ? rows : kDwChunkRows;
+    rows = rows < per ? rows : per;
     ti.nkb = rows > 0 ? (rows + kBK - 1) / kBK : 0;
     ti.split = nch > 1;
     ti.kb_half = ti.nkb;

@@ -58,7 +58,9 @@ enum class GemmKind : int { GateUp = 0, Down = 1, DA = 2, BwdGU = 3, Dx = 4, DwG
 // Tile sizes shared by host and device.
 constexpr int kBM = 128;        // token rows (or feature rows for dW) per tile
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
-constexpr int kDwChunkRows = 2048;  // tokens per dW split-K chunk
+// An expert with more padded rows than this is split into equal dW chunks of at most this
+// many rows (reduce-added) and gets the compensated (value + residual) fp16 operands.
+constexpr int kDwChunkRows = 4096;
 constexpr int kMaxExperts = 1024;   // largest E the entry points accept
 
 struct GemmParams {

@@ -579,45 +579,60 @@ cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, co
 }
 
 // ------------------------------------------------------------------ dW split-K preparation
-// Block 0 writes dw_prefix[e] = sum_{e' < e} chunks(e'), chunks(e) = max(1, ceil(rows_e / kDwChunkRows)).
+// Block (0,0) writes dw_prefix[e] = sum_{e' < e} chunks(e'), chunks(e) = max(1, ceil(rows_e / kDwChunkRows)).
 // Block e zeroes dW[e] when expert e is split (its tiles reduce-add into it).
-__global__ void __launch_bounds__(1024) k_dw_prep(const int32_t* __restrict__ offsets, int E,
-                                                  int* __restrict__ dw_prefix,
-                                                  float* __restrict__ dwg,
-                                                  float* __restrict__ dwu,
-                                                  float* __restrict__ dwd, int D, int I) {
+__global__ void __launch_bounds__(256) k_dw_prep(const int32_t* __restrict__ offsets, int E,
+                                                 int* __restrict__ dw_prefix,
+                                                 float* __restrict__ dwg,
+                                                 float* __restrict__ dwu,
+                                                 float* __restrict__ dwd, int D, int I) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    // chunks(e) = max(1, ceil(rows_e / kDwChunkRows)); each thread sums a run of experts
     __shared__ int s_warp[32];
-    const int e = threadIdx.x;
-    int ch = 0;
-    if (e < E) {
-      const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
-      ch = (rows + kDwChunkRows - 1) / kDwChunkRows;
-      if (ch < 1) ch = 1;
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = threadIdx.x * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
+        const int ch = (rows + kDwChunkRows - 1) / kDwChunkRows;
+        local += ch < 1 ? 1 : ch;
+      }
     }
-    const int incl = warp_incl_scan(ch, lane);
+    const int incl = warp_incl_scan(local, lane);
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-      const int v = s_warp[lane];
+      const int v = lane < static_cast<int>(blockDim.x >> 5) ? s_warp[lane] : 0;
       s_warp[lane] = warp_incl_scan(v, lane) - v;
     }
     __syncthreads();
-    const int excl = s_warp[warp] + incl - ch;
-    if (e < E) dw_prefix[e] = excl;
-    if (e == E - 1) dw_prefix[E] = excl + ch;
+    int run = s_warp[warp] + incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        dw_prefix[e] = run;
+        const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
+        const int ch = (rows + kDwChunkRows - 1) / kDwChunkRows;
+        run += ch < 1 ? 1 : ch;
+      }
+    }
+    if (threadIdx.x == blockDim.x - 1) dw_prefix[E] = run;
   }
   const int e = blockIdx.x;
   if (e >= E) return;
   const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
   if (rows <= kDwChunkRows) return;
+  // a split expert's three dW tensors are zeroed by gridDim.y blocks, one slice each
   const size_t n4 = static_cast<size_t>(D) * I / 4;
   float4* g4 = reinterpret_cast<float4*>(dwg + static_cast<size_t>(e) * D * I);
   float4* u4 = reinterpret_cast<float4*>(dwu + static_cast<size_t>(e) * D * I);
   float4* d4 = reinterpret_cast<float4*>(dwd + static_cast<size_t>(e) * D * I);
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (size_t i = threadIdx.x; i < n4; i += blockDim.x) {
+  const size_t step = static_cast<size_t>(blockDim.x) * gridDim.y;
+  for (size_t i = static_cast<size_t>(blockIdx.y) * blockDim.x + threadIdx.x; i < n4; i += step) {
     g4[i] = z;
     u4[i] = z;
     d4[i] = z;
@@ -627,7 +642,10 @@ __global__ void __launch_bounds__(1024) k_dw_prep(const int32_t* __restrict__ of
 cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float* dw_gate,
                            float* dw_up, float* dw_down, int D, int I, cudaStream_t s) {
   LaunchScope ls(kKDwPrep, s);
-  k_dw_prep<<<E, 1024, 0, s>>>(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I);
+  // ~2048 blocks in all, so that one split expert's zeroing still spans the GPU while a
+  // launch with no split expert stays cheap
+  const int slices = E >= 2048 ? 1 : 2048 / E;
+  k_dw_prep<<<dim3(E, slices), 256, 0, s>>>(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I);
   return cudaGetLastError();
 }
 
