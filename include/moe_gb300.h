@@ -151,7 +151,7 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *        dw_down[e] = sum_s (w act)_s^T dy_row_s,  dw_gate[e] = x_perm_e^T dG_e,
  *        dw_up[e] = x_perm_e^T dU_e
  *      computed from fp16 operands (x and dy convert exactly; the intermediates keep 10
- *      mantissa bits) with fp32 accumulation; experts with more than 2048 rows are split
+ *      mantissa bits) with fp32 accumulation; experts with more than 4096 rows are split
  *      over several tiles whose parts are TMA reduce-added.  Experts with no rows get
  *      exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
  *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets/counts (counts may be NULL) from
