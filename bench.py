@@ -34,6 +34,21 @@ GEMM_FLOPS_RDI = {"gemm_gateup_swiglu": 4, "gemm_down": 2, "gemm_dA": 2, "gemm_b
                   "gemm_dx": 4, "gemm_dw_gateup": 4, "gemm_dw_down": 2}
 
 
+def gemm_bytes(s):
+    """Algorithmic bytes per launch of each grouped GEMM: the expert weights it reads once,
+    the routed rows it reads and writes once (padding excluded), and its fp32 weight
+    gradients.  Rows: x and dY bf16 / fp16 (2 B), intermediates 2 B, dA fp16."""
+    R, D, I, E = s.R, s.D, s.I, s.E
+    w1 = E * D * I * 2          # one weight matrix, bf16
+    return {"gemm_gateup_swiglu": 2 * w1 + R * D * 2 + R * I * 2,
+            "gemm_down": w1 + R * I * 2 + R * D * 2,
+            "gemm_dA": w1 + R * D * 2 + R * I * 2,
+            "gemm_bwd_gateup": 2 * w1 + R * D * 2 + R * I * 2 + R * I * 2 + 2 * (R * 2 * I * 2),
+            "gemm_dx": 2 * w1 + R * 2 * I * 2 + R * D * 2,
+            "gemm_dw_gateup": R * D * 2 + R * 2 * I * 2 + 2 * E * D * I * 4,
+            "gemm_dw_down": R * I * 2 + R * D * 2 + E * I * D * 4}
+
+
 def movement_bytes(s):
     """Algorithmic bytes per launch of the HBM-bound kernels (what each must read and
     write at the minimum): permute (x rows in, sorted rows out, slot ids and weights),
@@ -452,14 +467,22 @@ def main():
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     rdi = s.R * s.D * s.I
     kernels = {}
+    hbm_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gb = gemm_bytes(s)
+    ridge = peak * 1e12 / (hbm_gbs * 1e9)   # FLOP per byte where the two roofs meet
     for k, (ms_k, n_k) in sorted(per_kernel.items()):
         ent = {"ms_per_launch": ms_k / n_k, "launches_per_step": n_k / kpass}
         if k in GEMM_FLOPS_RDI:
-            tf = GEMM_FLOPS_RDI[k] * rdi / (ms_k / n_k * 1e-3) / 1e12
+            sec = ms_k / n_k * 1e-3
+            tf = GEMM_FLOPS_RDI[k] * rdi / sec / 1e12
+            ai = GEMM_FLOPS_RDI[k] * rdi / gb[k]
             ent["tflops"] = tf
             ent["frac_of_sustained_peak"] = tf / peak
+            ent["gbs"] = gb[k] / sec / 1e9
+            ent["flop_per_byte"] = ai
+            ent["bound"] = "tensor" if ai >= ridge else "hbm"
+            ent["frac_of_roof"] = (tf / peak) if ai >= ridge else ent["gbs"] / hbm_gbs
         kernels[k] = ent
-    hbm_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     for k, nbytes in movement_bytes(s).items():
         if k in kernels:
             gbs = nbytes / (kernels[k]["ms_per_launch"] * 1e-3) / 1e9
@@ -469,10 +492,14 @@ def main():
     roof_fwd = min(peak_tf, s.fwd_flops() / db["fwd"] * hbm_gbs * 1e9 / 1e12)
     roof_bwd = min(peak_tf, s.bwd_flops() / db["bwd"] * hbm_gbs * 1e9 / 1e12)
     achieved = dom_ms = None
+    dom_bound = kernels[dom]["bound"] if dom else "tensor"
     if dom and dom in dom_timed:
         ms_d, n_d = dom_timed[dom]
         dom_ms = ms_d / n_d
-        achieved = GEMM_FLOPS_RDI[dom] * rdi / (dom_ms * 1e-3) / 1e12
+        if dom_bound == "tensor":
+            achieved = GEMM_FLOPS_RDI[dom] * rdi / (dom_ms * 1e-3) / 1e12
+        else:
+            achieved = gb[dom] / (dom_ms * 1e-3) / 1e9
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.json")
     if dom and os.path.exists(prof):
@@ -509,11 +536,18 @@ def main():
                   "value": job_throughput(step_flops, world, graph_ms * 1e-3) / 1e12,
                   "note": "the same step captured once as a CUDA graph and replayed"},
         "step_ms_median": statistics.median(step_ms),
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved,
-                     "ms_per_launch": dom_ms,
-                     "peak": peak, "unit": "TFLOP/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": traffic,
-                     "peak_source": f"bf16_tflops_sustained ({peak_src})"},
+        "roofline": ({"kernel": dom, "bound": "tensor", "achieved": achieved,
+                      "ms_per_launch": dom_ms, "peak": peak, "unit": "TFLOP/s",
+                      "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                      "peak_source": f"bf16_tflops_sustained ({peak_src})"}
+                     if dom_bound == "tensor" else
+                     {"kernel": dom, "bound": "hbm", "achieved": achieved,
+                      "ms_per_launch": dom_ms, "peak": hbm_gbs, "unit": "GB/s",
+                      "frac": (achieved / hbm_gbs) if achieved else None, "traffic": traffic,
+                      "algorithmic_bytes": gb[dom],
+                      "flop_per_byte": kernels[dom]["flop_per_byte"],
+                      "tflops": GEMM_FLOPS_RDI[dom] * rdi / (dom_ms * 1e-3) / 1e12 if dom_ms else None,
+                      "peak_source": f"hbm_gbs ({peak_src})"}),
         "kernels": kernels,
         "kernels_pass": f"separate pass of {kpass} steps before the timed region, every "
                         "launch bracketed by CUDA events",
