@@ -353,8 +353,7 @@ def main():
     # Every step copies its inputs (x, ids, w, dY) in from pinned host memory and its
     # results (Y, dX) out.  The copies run on a second stream and are double-buffered:
     # step i+2's inputs are copied in and step i's results copied out while step i+1
-    # computes (results are first staged in device buffers so the next step may reuse the
-    # layer's own output tensors).
+    # computes (the layer writes Y and dX into one of two device output sets).
     keys = ("x", "topk_ids", "topk_w", "dy")
     host = {k: inp[k].cpu().pin_memory() for k in keys}
     out_y = [torch.empty(s.T, s.D, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -378,11 +377,9 @@ def main():
         b = i % 2
         stream.wait_event(h2d_done[b])
         d = dev_in[b]
-        y = layer.forward(d["x"], d["topk_ids"], d["topk_w"], wg, wu, wd)
-        dx = layer.backward(d["dy"], wg, wu, wd)[0]
-        stream.wait_event(d2h_done[b])          # staging slot b has been copied out
-        stage_y[b].copy_(y)
-        stage_dx[b].copy_(dx)
+        stream.wait_event(d2h_done[b])          # output set b has been copied out
+        layer.forward(d["x"], d["topk_ids"], d["topk_w"], wg, wu, wd, out=stage_y[b])
+        layer.backward(d["dy"], wg, wu, wd, dx_out=stage_dx[b])
         staged[b].record(stream)
         with torch.cuda.stream(copy):
             copy.wait_event(staged[b])
@@ -418,6 +415,7 @@ def main():
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_value = job_throughput(step_flops, world, e2e_ms / args.steps * 1e-3) / 1e12
     assert layer.device_error()[0] == B.MOE_OK
+    # the host copy of the last step's Y equals the device-resident result of the same inputs
     assert torch.equal(out_y[(args.steps - 1) % 2].to(dev), layer.y)
 
     # ---------------- the same step captured once as a CUDA graph and replayed

@@ -52,27 +52,30 @@ class MoEExpertMLP:
         self._topk_w = None
         self._x = None
 
-    def forward(self, x, topk_ids, topk_w, w_gate, w_up, w_down, stream=None):
-        """Y [T, D] bf16 = sum_k topk_w[t,k] * SwiGLU-MLP_{topk_ids[t,k]}(x[t])."""
+    def forward(self, x, topk_ids, topk_w, w_gate, w_up, w_down, stream=None, out=None):
+        """Y [T, D] bf16 = sum_k topk_w[t,k] * SwiGLU-MLP_{topk_ids[t,k]}(x[t]), written to
+        `out` if given (else to the layer's own buffer)."""
         T, K, E, D, I, a = self.T, self.K, self.E, self.D, self.I, self.align
         B.moe_route_permute(topk_ids, topk_w, x, T, K, E, D, a, self.counts, self.offsets,
                             self.perm_src, self.inv_perm, self.w_perm, self.x_perm,
                             self.workspace, stream)
         B.moe_expert_mlp_fwd(self.x_perm, w_gate, w_up, w_down, self.offsets, self._counts(), T,
                              K, E, D, I, a, self.y_perm, self.workspace, stream)
-        B.moe_combine(self.y_perm, self.inv_perm, topk_w, T, K, D, self.y, stream)
+        y = self.y if out is None else out
+        B.moe_combine(self.y_perm, self.inv_perm, topk_w, T, K, D, y, stream)
         self._x = x   # the backward gathers its fp16 copy of the sorted rows from x
-        return self.y
+        return y
 
-    def backward(self, dy, w_gate, w_up, w_down, stream=None):
+    def backward(self, dy, w_gate, w_up, w_down, stream=None, dx_out=None):
         """(dX [T,D] bf16, dW_gate [E,D,I] f32, dW_up [E,D,I] f32, dW_down [E,I,D] f32)
         of L = sum(Y * dy), for the routing of the last forward."""
         T, K, E, D, I, a = self.T, self.K, self.E, self.D, self.I, self.align
         B.moe_expert_mlp_bwd(dy, self._x, self.x_perm, self.perm_src, self.w_perm, self.offsets,
                              self._counts(), w_gate, w_up, w_down, T, K, E, D, I, a, self.dx_perm,
                              self.dw_gate, self.dw_up, self.dw_down, self.workspace, stream)
-        B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, self.dx, stream)
-        return self.dx, self.dw_gate, self.dw_up, self.dw_down
+        dx = self.dx if dx_out is None else dx_out
+        B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, dx, stream)
+        return dx, self.dw_gate, self.dw_up, self.dw_down
 
     def route(self, logits, router="softmax", stream=None):
         """(topk_ids [T,K] int32, topk_w [T,K] fp32) from router logits [T,E] fp32."""
