@@ -46,9 +46,9 @@ def random_layer(T, D, I, E, K, seed, ids=None, w_std=0.02):
     return dict(x=x, w_gate=wg, w_up=wu, w_down=wd, dy=dy, topk_ids=ids, topk_w=w.float())
 
 
-def run_gpu(inp, T, D, I, E, K):
+def run_gpu(inp, T, D, I, E, K, align=128):
     g = {k: v.to(DEV) for k, v in inp.items()}
-    layer = MoEExpertMLP(T, K, E, D, I, align=128, device=DEV)
+    layer = MoEExpertMLP(T, K, E, D, I, align=align, device=DEV)
     y = layer.forward(g["x"], g["topk_ids"], g["topk_w"], g["w_gate"], g["w_up"], g["w_down"])
     dx, dwg, dwu, dwd = layer.backward(g["dy"], g["w_gate"], g["w_up"], g["w_down"])
     torch.cuda.synchronize()
@@ -57,11 +57,11 @@ def run_gpu(inp, T, D, I, E, K):
     return layer
 
 
-def check_full(inp, T, D, I, E, K):
-    layer = run_gpu(inp, T, D, I, E, K)
+def check_full(inp, T, D, I, E, K, align=128):
+    layer = run_gpu(inp, T, D, I, E, K, align)
     x, wg, wu, wd, dy, w = (f64(inp[k]) for k in ("x", "w_gate", "w_up", "w_down", "dy", "topk_w"))
     ids = i64(inp["topk_ids"])
-    r = oracle.route_permute(ids, w, x, E, 128)
+    r = oracle.route_permute(ids, w, x, E, align)
     used = int(r["offsets"][-1])
     assert np.array_equal(i64(layer.offsets), r["offsets"])
     # per-call parity: expert MLP forward on the oracle's own sorted rows
@@ -99,9 +99,18 @@ def test_tiny_layer():
     (300, 768, 256, 3, 3, 3),     # D = 3 x 256, I = 2 x 128
     (200, 256, 128, 1, 1, 4),     # a single expert
     (512, 256, 128, 256, 8, 5),   # many experts with a handful of rows each (mostly padding)
+    (64, 256, 128, 1024, 32, 6),  # the largest expert count and top-K
 ])
 def test_small_layers(T, D, I, E, K, seed):
     check_full(random_layer(T, D, I, E, K, seed), T, D, I, E, K)
+
+
+@pytest.mark.parametrize("align", [256, 384])
+def test_coarser_padding(align):
+    """Experts padded to 256 or 384 rows: every expert then spans whole row pairs (256)
+    or one and a half (384: an odd tile count whose last tile is padding)."""
+    T, D, I, E, K = 500, 256, 256, 6, 2
+    check_full(random_layer(T, D, I, E, K, seed=14), T, D, I, E, K, align=align)
 
 
 @pytest.mark.parametrize("I", [256, 384])
