@@ -96,11 +96,10 @@ def load_peaks():
 
 def get_shape(name):
     from mixture_experts_expert_gb300 import synth
-    if name in synth.SHAPES:
-        return synth.SHAPES[name]
-    if name.startswith("qwen3_30b_a3b_T"):
-        return synth.sweep_shape(int(name.split("_T")[-1]))
-    raise SystemExit(f"unknown workload {name}")
+    try:
+        return synth.shape_by_name(name)
+    except ValueError as e:
+        raise SystemExit(str(e))
 
 
 class ClockSampler:
@@ -558,6 +557,8 @@ def main():
                                       (router_ms.get("router_weight_grad", float("nan")) * 1e-3) / 1e9,
                    "note": "router step, outside the expert-MLP metric"},
     }
+    tun, tun_src = B.moe_tuning_get(s.T, s.K, s.E, s.D, s.I)
+    line["tuning"] = {"source": tun_src, **tun}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s)
     print(json.dumps(line), flush=True)

@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 typedef uint16_t moe_bf16_t;
 
@@ -250,6 +250,58 @@ int moe_route_permute_noalloc(const int32_t* topk_ids, const float* topk_w,
  * moe_workspace_init, before reusing a workspace after an error.  For tests and debugging.
  */
 int moe_get_device_error(void* workspace, int* code, int* detail, void* stream);
+
+/* ---- per-shape tuning -------------------------------------------------------
+ * Launch choices of the grouped GEMMs that change their speed, not what they compute
+ * (results stay within the same tolerance of the exact values; the tile order changes no
+ * bit at all).  A table compiled into the library, written by the package's tuner from
+ * measurements on a GB300, picks them per layer shape; shapes it does not hold get the
+ * defaults.  The pages rely on tuned per-shape configurations in the same way
+ * ("LigerCute -- native CUTLASS + NVSHMEM kernels", the tuned kernel-configuration tables
+ * of the grouped GEMMs). */
+
+/* Token-row grouped GEMMs, as indices of moe_tuning_t.order. */
+typedef enum {
+  MOE_GEMM_GATE_UP = 0,      /* forward gate/up + SwiGLU */
+  MOE_GEMM_DOWN = 1,         /* forward down projection */
+  MOE_GEMM_DA = 2,           /* backward dA = w * dY W_down^T */
+  MOE_GEMM_BWD_GATE_UP = 3,  /* backward gate/up recompute + SwiGLU' */
+  MOE_GEMM_DX = 4            /* backward dX */
+} moe_tuned_gemm_t;
+
+typedef struct {
+  /* Per token-row GEMM: the order of an expert's tiles.  0 (default): row pair by row
+   * pair, its N tiles consecutive (they share the token rows); 1: N tile by N tile, its
+   * row pairs consecutive (they share each weight tile; pays when an expert's weights are
+   * large and it has several 256-row pairs). */
+  int order[5];
+  /* 1 (default): an expert's odd last 128-row tile is computed transposed, over its real
+   * rows only; 0: as half of a 256-row pair whose other half idles. */
+  int swap_tails;
+  /* dA GEMM output columns per tile: 256 (the default when I % 256 == 0) or 128.  256 on
+   * a shape with I % 256 != 0 runs as 128. */
+  int da_tile_n;
+  /* An expert with more padded rows than this has its weight gradient split into equal
+   * chunks of at most this many rows, reduce-added in fp32, with compensated fp16
+   * operands.  A multiple of 64 in [256, 65536]; default 4096. */
+  int dw_chunk_rows;
+} moe_tuning_t;
+
+/*
+ * The choices moe_expert_mlp_fwd / moe_expert_mlp_bwd make for this shape.  Host only
+ * (needs no GPU).  *source (if not NULL) receives 0 = defaults, 1 = the compiled table
+ * (the entry with the same K, E, D, I and the nearest T), 2 = the override.
+ * MOE_ERR_INVALID_ARG for a NULL `out` or sizes outside the entry points' ranges.
+ */
+int moe_tuning_get(int T, int K, int E, int D, int I, moe_tuning_t* out, int* source);
+
+/*
+ * Process-wide override: every later moe_expert_mlp_fwd / _bwd call, of any shape, uses
+ * `t` until a call with NULL returns to the table.  For tuners and tests.  A value out of
+ * range returns MOE_ERR_INVALID_ARG and leaves the previous state.  Calls read the
+ * setting once, when they launch: change it only between calls.
+ */
+int moe_tuning_override(const moe_tuning_t* t);
 
 /* ---- diagnostics ---------------------------------------------------------- */
 

@@ -36,6 +36,16 @@ _lib = None
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
+
+# moe_tuned_gemm_t: index of each token-row GEMM in moe_tuning_t.order
+TUNED_GEMMS = ("gate_up", "down", "dA", "bwd_gate_up", "dx")
+TUNING_SOURCES = ("default", "table", "override")
+
+
+class MoeTuning(ctypes.Structure):
+    _fields_ = [("order", _I * 5), ("swap_tails", _I), ("da_tile_n", _I),
+                ("dw_chunk_rows", _I)]
+
 _SIGS = {
     "moe_abi_version": (_I, []),
     "moe_status_string": (ctypes.c_char_p, [_I]),
@@ -59,6 +69,8 @@ _SIGS = {
     "moe_router_weight_grad": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_router_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_timing_enable_mask": (_I, [ctypes.c_ulonglong]),
+    "moe_tuning_get": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(MoeTuning), ctypes.POINTER(_I)]),
+    "moe_tuning_override": (_I, [ctypes.POINTER(MoeTuning)]),
     "moe_timing_collect": (_I, [ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -265,6 +277,36 @@ def moe_timing_enable_only(names):
     for n in names:
         mask |= 1 << ids.index(n)
     _check("moe_timing_enable_mask", lib().moe_timing_enable_mask(mask))
+
+
+def _tuning_dict(t: MoeTuning) -> dict:
+    return {"order": {g: t.order[i] for i, g in enumerate(TUNED_GEMMS)},
+            "swap_tails": t.swap_tails, "da_tile_n": t.da_tile_n,
+            "dw_chunk_rows": t.dw_chunk_rows}
+
+
+def moe_tuning_get(T: int, K: int, E: int, D: int, I: int):
+    """(choices, source) the forward/backward calls of this shape use; host only."""
+    t, src = MoeTuning(), ctypes.c_int(0)
+    _check("moe_tuning_get", lib().moe_tuning_get(T, K, E, D, I, ctypes.byref(t),
+                                                   ctypes.byref(src)))
+    return _tuning_dict(t), TUNING_SOURCES[src.value]
+
+
+def moe_tuning_override(choices=None):
+    """Sets the process-wide override (a dict shaped like moe_tuning_get's), or clears it
+    (None).  Missing keys take the defaults."""
+    if choices is None:
+        _check("moe_tuning_override", lib().moe_tuning_override(None))
+        return
+    t = MoeTuning()
+    order = choices.get("order", {})
+    for i, g in enumerate(TUNED_GEMMS):
+        t.order[i] = int(order.get(g, 0))
+    t.swap_tails = int(choices.get("swap_tails", 1))
+    t.da_tile_n = int(choices.get("da_tile_n", 256))
+    t.dw_chunk_rows = int(choices.get("dw_chunk_rows", 4096))
+    _check("moe_tuning_override", lib().moe_tuning_override(ctypes.byref(t)))
 
 
 def moe_timing_collect():

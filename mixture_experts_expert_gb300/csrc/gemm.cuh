@@ -20,7 +20,11 @@
 //
 // Tiles are scheduled statically (tile = cta (or pair) index + i * count) over a tile space
 // whose size is read on the device from the expert offsets, so the launch is
-// independent of the routing (no host sync; valid inside a captured CUDA graph).
+// independent of the routing (no host sync; valid inside a captured CUDA graph).  Within
+// an expert the pair kinds enumerate tiles row pair by row pair (consecutive tiles share
+// the token rows) or, per the shape's tuning, N tile by N tile (consecutive tiles share a
+// weight tile: better when an expert's weights are large and it has several row pairs).
+// Odd last row tiles are computed transposed unless the tuning turns that off.
 //
 // Kinds (row-major; "perm" rows are expert-sorted, padded to 128 rows per expert):
 //   GateUp  act[s, i]  = silu(x_perm[s] W_g[e])_i * (x_perm[s] W_u[e])_i   N: 128 gate + 128 up
@@ -36,7 +40,7 @@
 // The weight-gradient GEMMs sum over up to thousands of token rows, so their operands
 // are fp16 (10-bit mantissa; x and dY convert exactly) rather than bf16: the rounding of
 // the intermediates (dG, dU, w*act) is what bounds dW's absolute error.  dW tiles cover
-// at most kDwChunkRows token rows; an expert with more rows is split into equal chunks on
+// at most dw_chunk_rows token rows; an expert with more rows is split into equal chunks on
 // tiles whose fp32 results are TMA reduce-added into a zeroed dW, and its rows run twice
 // (values, then residuals) so that its error does not grow with the row count.
 #pragma once
@@ -194,12 +198,21 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, cons
       ti.e = find_segment_smem(pfx, p.E, nt_all);
       const int beg = __ldg(p.offsets + ti.e);
       const int mt = (__ldg(p.offsets + ti.e + 1) - beg) / kBM;
-      const int j = nt_all - pfx[ti.e];
+      int j = nt_all - pfx[ti.e];
+      if (p.order == 1) {
+        // the expert's tiles N tile by N tile: its row pairs share each weight tile back to back
+        const int np = pfx[ti.e + 1] - pfx[ti.e];
+        const int l = t - pfx[ti.e] * p.n_tiles;
+        const int n_idx = l / np;
+        j = l - n_idx * np;
+        ti.n0 = n_idx * (KIND == GemmKind::DA ? p.tile_n : KindTraits<KIND>::kTileN);
+      }
       // An odd last row tile has no partner tile: the pair computes it transposed
       // (weights as the M = 256 operand, its token rows as N), so only its real rows,
       // rounded up to 32, cost MMA time.  DA with 128-column tiles has no M = 256 form of
       // the swap and runs the tile with an idle (ghost) odd half instead.
-      if ((mt & 1) && 2 * j + 1 == mt && (KIND != GemmKind::DA || p.tile_n == 256)) {
+      if (p.swap_tails && (mt & 1) && 2 * j + 1 == mt &&
+          (KIND != GemmKind::DA || p.tile_n == 256)) {
         ti.swap = 1;
         ti.m0 = beg + (mt - 1) * kBM;
         int rows = kBM;
@@ -613,7 +626,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
     return true;
   } else if constexpr (KIND == GemmKind::DA) {
     const int x = ti.n0 + 128 * rank + 32 * q;
-    const bool want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
+    const bool want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
     for (int j = 0; j < nch; ++j) {
       const float wl = __ldg(p.w_perm + ti.m0 + 32 * j + lane);   // router weight of row lane
       uint32_t r[32];
@@ -671,7 +684,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
     const int f0 = ti.n0 + 64 * rank + 32 * pi;
     bool want_lo = false;
     if constexpr (KIND == GemmKind::BwdGU)
-      want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
+      want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
     for (int j = 0; j < nch; ++j) {
       const int row0 = ti.m0 + 32 * j;
       uint32_t g[32];
@@ -882,7 +895,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
       } else if constexpr (KIND == GemmKind::DA) {
         const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
         const bool want_lo =
-            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
+            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
         const int nch = p.tile_n / 32;
         for (int c = 0; c < nch; ++c) {
           uint32_t r[32];
@@ -910,7 +923,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         const float wr = __ldg(p.w_perm + my_row);
         // rows of an expert whose dW is split over several tiles also get the fp16 residuals
         const bool want_lo =
-            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > kDwChunkRows;
+            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
         const uint4* da_row =
             reinterpret_cast<const uint4*>(p.dA + static_cast<size_t>(my_row) * p.I + ti.n0);
         const uint4* dl_row =

@@ -58,8 +58,9 @@ enum class GemmKind : int { GateUp = 0, Down = 1, DA = 2, BwdGU = 3, Dx = 4, DwG
 // Tile sizes shared by host and device.
 constexpr int kBM = 128;        // token rows (or feature rows for dW) per tile
 constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle row of bf16)
-// An expert with more padded rows than this is split into equal dW chunks of at most this
-// many rows (reduce-added) and gets the compensated (value + residual) fp16 operands.
+// Default dW chunk: an expert with more padded rows than the chunk size is split into equal
+// dW chunks of at most that many rows (reduce-added) and gets the compensated
+// (value + residual) fp16 operands.  The per-shape tuning may choose another multiple of 64.
 constexpr int kDwChunkRows = 4096;
 constexpr int kMaxExperts = 1024;   // largest E the entry points accept
 
@@ -86,6 +87,10 @@ struct GemmParams {
   int n_tiles;             // N tiles per M tile
   int m_tiles;             // M tiles per expert (dW kinds)
   int tile_n;              // DA: output columns per tile (256, or 128 when I % 256 != 0)
+  int order;               // pair kinds: 0 = an expert's tiles row pair by row pair (N tiles
+                           // consecutive), 1 = N tile by N tile (row pairs consecutive)
+  int swap_tails;          // pair kinds: odd last row tiles computed transposed (else a ghost half)
+  int dw_chunk_rows;       // dW split threshold / chunk size (multiple of 64)
   int drop_loads;          // test hook: the producer issues nothing, so the waits expire
 };
 
@@ -114,8 +119,9 @@ cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const ui
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
                            int T, int K, int D, uint16_t* out, cudaStream_t s);
 
-cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float* dw_gate,
-                           float* dw_up, float* dw_down, int D, int I, cudaStream_t s);
+cudaError_t launch_dw_prep(const int32_t* offsets, int E, int chunk_rows, int* dw_prefix,
+                           float* dw_gate, float* dw_up, float* dw_down, int D, int I,
+                           cudaStream_t s);
 
 int route_num_chunks(int R);
 

@@ -242,6 +242,70 @@ static int take_drop_flag() {
   return d ? 1 : 0;
 }
 
+// ------------------------------------------------------------------ per-shape tuning
+struct TuneEntry {
+  int T, K, E, D, I;
+  int order[5];
+  int swap_tails, da_tile_n, dw_chunk_rows;
+};
+
+static const TuneEntry kTuneTable[] = {
+#include "tuning_table.inc"
+};
+
+static moe_tuning_t default_tuning() {
+  moe_tuning_t t{};
+  for (int i = 0; i < 5; ++i) t.order[i] = 0;
+  t.swap_tails = 1;
+  t.da_tile_n = 256;
+  t.dw_chunk_rows = kDwChunkRows;
+  return t;
+}
+
+static bool tuning_ok(const moe_tuning_t& t) {
+  for (int i = 0; i < 5; ++i)
+    if (t.order[i] != 0 && t.order[i] != 1) return false;
+  return (t.swap_tails == 0 || t.swap_tails == 1) && (t.da_tile_n == 128 || t.da_tile_n == 256) &&
+         t.dw_chunk_rows >= 256 && t.dw_chunk_rows <= 65536 && t.dw_chunk_rows % kBK == 0;
+}
+
+static std::mutex g_tune_mu;
+static bool g_tune_override_on = false;
+static moe_tuning_t g_tune_override;
+
+// The override if set; else the table entry of the same K, E, D, I with the nearest T
+// (by ratio; ties: the smaller T); else the defaults.
+static moe_tuning_t select_tuning(int T, int K, int E, int D, int I, int* source) {
+  {
+    std::lock_guard<std::mutex> g(g_tune_mu);
+    if (g_tune_override_on) {
+      if (source) *source = 2;
+      return g_tune_override;
+    }
+  }
+  const TuneEntry* best = nullptr;
+  double best_d = 0.0;
+  const double tq = T > 0 ? static_cast<double>(T) : 1.0;
+  for (const TuneEntry& en : kTuneTable) {
+    if (en.T <= 0 || en.K != K || en.E != E || en.D != D || en.I != I) continue;
+    const double r = tq > en.T ? tq / en.T : en.T / tq;
+    if (!best || r < best_d || (r == best_d && en.T < best->T)) {
+      best = &en;
+      best_d = r;
+    }
+  }
+  moe_tuning_t t = default_tuning();
+  if (best) {
+    for (int i = 0; i < 5; ++i) t.order[i] = best->order[i];
+    t.swap_tails = best->swap_tails;
+    t.da_tile_n = best->da_tile_n;
+    t.dw_chunk_rows = best->dw_chunk_rows;
+    if (!tuning_ok(t)) t = default_tuning();
+  }
+  if (source) *source = best ? 1 : 0;
+  return t;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -339,12 +403,16 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // token-row GEMMs run on CTA pairs: at most (row tiles + E) / 2 pairs of 256 rows
   const int pairs_max = static_cast<int>((cap / kBM + E + 1) / 2);
+  const moe_tuning_t tun = select_tuning(T, K, E, D, I, nullptr);
 
   GemmParams p{};
   p.offsets = offsets;
   p.counts = counts;
   p.err = reinterpret_cast<int*>(ws);
   p.E = E; p.D = D; p.I = I;
+  p.order = tun.order[MOE_GEMM_GATE_UP];
+  p.swap_tails = tun.swap_tails;
+  p.dw_chunk_rows = tun.dw_chunk_rows;
   // gate/up + SwiGLU (A1, B2, B3: the token rows and one-atom weight boxes of the
   // swapped tail tiles)
   bool ok = map_kmajor(&p.mapA0, x_perm, D, cap, 128) &&
@@ -369,6 +437,9 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   q.counts = counts;
   q.err = p.err;
   q.E = E; q.D = D; q.I = I;
+  q.order = tun.order[MOE_GEMM_DOWN];
+  q.swap_tails = tun.swap_tails;
+  q.dw_chunk_rows = tun.dw_chunk_rows;
   ok = map_kmajor(&q.mapA0, act, I, cap, 128) && map_kmajor(&q.mapA1, act, I, cap, 64) &&
        map_mnmajor(&q.mapB0, w_down, D, static_cast<uint64_t>(E) * I, 2) &&
        map_store_16(&q.mapO0, y_perm, D, cap);
@@ -413,6 +484,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   int* dw_prefix = reinterpret_cast<int*>(ws + L.dw_prefix);
   const int pairs_max = static_cast<int>((cap / kBM + E + 1) / 2);
   const uint64_t ED = static_cast<uint64_t>(E) * D, EI = static_cast<uint64_t>(E) * I;
+  const moe_tuning_t tun = select_tuning(T, K, E, D, I, nullptr);
+  const int chunk = tun.dw_chunk_rows;
   cudaError_t e;
 
   void* dh16 = ws + L.dh16;
@@ -434,7 +507,10 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   GemmParams da{};
   da.offsets = offsets; da.counts = counts; da.w_perm = w_perm; da.err = err;
   da.E = E; da.D = D; da.I = I;
-  da.tile_n = (I % 256 == 0) ? 256 : 128;
+  da.order = tun.order[MOE_GEMM_DA];
+  da.swap_tails = tun.swap_tails;
+  da.dw_chunk_rows = chunk;
+  da.tile_n = (tun.da_tile_n == 256 && I % 256 == 0) ? 256 : 128;
   bool ok = map_kmajor(&da.mapA0, dyp, D, cap, 128) && map_kmajor(&da.mapA1, dyp, D, cap, 64) &&
             map_kmajor(&da.mapB0, w_down, D, EI, static_cast<uint32_t>(da.tile_n / 2)) &&
             map_store_16(&da.mapO0, dA, I, cap, Elem::F16) &&
@@ -450,6 +526,9 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   a.offsets = offsets; a.counts = counts; a.w_perm = w_perm; a.dA = dA; a.dA_lo = dA_lo;
   a.err = err;
   a.E = E; a.D = D; a.I = I;
+  a.order = tun.order[MOE_GEMM_BWD_GATE_UP];
+  a.swap_tails = tun.swap_tails;
+  a.dw_chunk_rows = chunk;
   ok = map_kmajor(&a.mapA0, x_perm, D, cap, 128) && map_kmajor(&a.mapA1, x_perm, D, cap, 64) &&
        map_mnmajor(&a.mapB0, w_gate, I, ED, 2) && map_mnmajor(&a.mapB1, w_up, I, ED, 2) &&
        map_mnmajor(&a.mapB2, w_gate, I, ED, 1) && map_mnmajor(&a.mapB3, w_up, I, ED, 1) &&
@@ -469,6 +548,9 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   // 3. input gradient
   GemmParams xg{};
   xg.offsets = offsets; xg.counts = counts; xg.err = err; xg.E = E; xg.D = D; xg.I = I;
+  xg.order = tun.order[MOE_GEMM_DX];
+  xg.swap_tails = tun.swap_tails;
+  xg.dw_chunk_rows = chunk;
   ok = map_kmajor(&xg.mapA0, dh, 2ull * I, cap, 128) && map_kmajor(&xg.mapA1, dh, 2ull * I, cap, 64) &&
        map_kmajor(&xg.mapB0, w_gate, I, ED, 128) &&
        map_kmajor(&xg.mapB1, w_up, I, ED, 128) && map_store_16(&xg.mapO0, dx_perm, D, cap);
@@ -481,12 +563,13 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 4. weight gradients (fp16 operands, fp32 accumulate and output)
-  e = launch_dw_prep(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I, s);
+  e = launch_dw_prep(offsets, E, chunk, dw_prefix, dw_gate, dw_up, dw_down, D, I, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  const int max_chunks = E + static_cast<int>(cap / kDwChunkRows) + 1;
+  const int max_chunks = E + static_cast<int>(cap / chunk) + 1;
   GemmParams g{};
   g.offsets = offsets; g.counts = counts; g.dw_prefix = dw_prefix; g.err = err;
   g.E = E; g.D = D; g.I = I;
+  g.dw_chunk_rows = chunk;
   ok = map_mnmajor(&g.mapA0, xp16, D, cap, 2, Elem::F16) &&
        map_mnmajor(&g.mapB0, dh16, 2ull * I, cap, 4, Elem::F16) &&
        map_mnmajor(&g.mapB1, dh16_lo, 2ull * I, cap, 4, Elem::F16) &&
@@ -502,6 +585,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   GemmParams d{};
   d.offsets = offsets; d.counts = counts; d.dw_prefix = dw_prefix; d.err = err;
   d.E = E; d.D = D; d.I = I;
+  d.dw_chunk_rows = chunk;
   ok = map_mnmajor(&d.mapA0, act, I, cap, 2, Elem::F16) &&
        map_mnmajor(&d.mapA1, act_lo, I, cap, 2, Elem::F16) &&
        map_mnmajor(&d.mapB0, dyp16, D, cap, 4, Elem::F16) &&
@@ -514,6 +598,25 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
     e = launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, f->num_sms, s);
   }
   return to_status(e);
+}
+
+MOE_EXPORT int moe_tuning_get(int T, int K, int E, int D, int I, moe_tuning_t* out,
+                              int* source) {
+  if (!out || !basic_sizes_ok(T, K, E, 128) || D < 1 || I < 1) return MOE_ERR_INVALID_ARG;
+  *out = select_tuning(T, K, E, D, I, source);
+  return MOE_OK;
+}
+
+MOE_EXPORT int moe_tuning_override(const moe_tuning_t* t) {
+  std::lock_guard<std::mutex> g(g_tune_mu);
+  if (!t) {
+    g_tune_override_on = false;
+    return MOE_OK;
+  }
+  if (!tuning_ok(*t)) return MOE_ERR_INVALID_ARG;
+  g_tune_override = *t;
+  g_tune_override_on = true;
+  return MOE_OK;
 }
 
 static bool router_args_ok(int T, int E, int K, int router) {

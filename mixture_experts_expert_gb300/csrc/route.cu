@@ -579,16 +579,16 @@ cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, co
 }
 
 // ------------------------------------------------------------------ dW split-K preparation
-// Block (0,0) writes dw_prefix[e] = sum_{e' < e} chunks(e'), chunks(e) = max(1, ceil(rows_e / kDwChunkRows)).
+// Block (0,0) writes dw_prefix[e] = sum_{e' < e} chunks(e'), chunks(e) = max(1, ceil(rows_e / chunk)).
 // Block e zeroes dW[e] when expert e is split (its tiles reduce-add into it).
 __global__ void __launch_bounds__(256) k_dw_prep(const int32_t* __restrict__ offsets, int E,
-                                                 int* __restrict__ dw_prefix,
+                                                 int chunk, int* __restrict__ dw_prefix,
                                                  float* __restrict__ dwg,
                                                  float* __restrict__ dwu,
                                                  float* __restrict__ dwd, int D, int I) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x == 0 && blockIdx.y == 0) {
-    // chunks(e) = max(1, ceil(rows_e / kDwChunkRows)); each thread sums a run of experts
+    // chunks(e) = max(1, ceil(rows_e / chunk)); each thread sums a run of experts
     __shared__ int s_warp[32];
     const int per = (E + blockDim.x - 1) / blockDim.x;
     const int e0 = threadIdx.x * per;
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(256) k_dw_prep(const int32_t* __restrict__ off
       const int e = e0 + i;
       if (e < E) {
         const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
-        const int ch = (rows + kDwChunkRows - 1) / kDwChunkRows;
+        const int ch = (rows + chunk - 1) / chunk;
         local += ch < 1 ? 1 : ch;
       }
     }
@@ -615,7 +615,7 @@ __global__ void __launch_bounds__(256) k_dw_prep(const int32_t* __restrict__ off
       if (e < E) {
         dw_prefix[e] = run;
         const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
-        const int ch = (rows + kDwChunkRows - 1) / kDwChunkRows;
+        const int ch = (rows + chunk - 1) / chunk;
         run += ch < 1 ? 1 : ch;
       }
     }
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(256) k_dw_prep(const int32_t* __restrict__ off
   const int e = blockIdx.x;
   if (e >= E) return;
   const int rows = __ldg(offsets + e + 1) - __ldg(offsets + e);
-  if (rows <= kDwChunkRows) return;
+  if (rows <= chunk) return;
   // a split expert's three dW tensors are zeroed by gridDim.y blocks, one slice each
   const size_t n4 = static_cast<size_t>(D) * I / 4;
   float4* g4 = reinterpret_cast<float4*>(dwg + static_cast<size_t>(e) * D * I);
@@ -639,13 +639,15 @@ __global__ void __launch_bounds__(256) k_dw_prep(const int32_t* __restrict__ off
   }
 }
 
-cudaError_t launch_dw_prep(const int32_t* offsets, int E, int* dw_prefix, float* dw_gate,
-                           float* dw_up, float* dw_down, int D, int I, cudaStream_t s) {
+cudaError_t launch_dw_prep(const int32_t* offsets, int E, int chunk_rows, int* dw_prefix,
+                           float* dw_gate, float* dw_up, float* dw_down, int D, int I,
+                           cudaStream_t s) {
   LaunchScope ls(kKDwPrep, s);
   // ~2048 blocks in all, so that one split expert's zeroing still spans the GPU while a
   // launch with no split expert stays cheap
   const int slices = E >= 2048 ? 1 : 2048 / E;
-  k_dw_prep<<<dim3(E, slices), 256, 0, s>>>(offsets, E, dw_prefix, dw_gate, dw_up, dw_down, D, I);
+  k_dw_prep<<<dim3(E, slices), 256, 0, s>>>(offsets, E, chunk_rows, dw_prefix, dw_gate, dw_up,
+                                             dw_down, D, I);
   return cudaGetLastError();
 }
 

@@ -89,6 +89,15 @@ SHAPES = {s.name: s for s in (TINY, QWEN3_30B_A3B, LLAMA4_SCOUT, SKEWED, SKEWED_
                                SCOUT_SKEWED)}
 
 
+def shape_by_name(name: str) -> MoEShape:
+    """A workload of SHAPES, or a sweep point ``qwen3_30b_a3b_T<T>``."""
+    if name in SHAPES:
+        return SHAPES[name]
+    if name.startswith("qwen3_30b_a3b_T"):
+        return sweep_shape(int(name.split("_T")[-1]))
+    raise ValueError(f"unknown workload {name!r}")
+
+
 def route_from_logits(logits: torch.Tensor, K: int, router: str):
     """Top-K expert ids (int32) and fp32 router weights from fp32 logits."""
     if router == "softmax":

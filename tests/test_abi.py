@@ -34,7 +34,7 @@ def test_library_is_sm103a_only():
 
 
 def test_abi_version_and_status_strings(lib):
-    assert B.moe_abi_version() == 3
+    assert B.moe_abi_version() == 4
     assert B.moe_status_string(0) == "ok"
     assert "invalid" in B.moe_status_string(-1)
     assert B.moe_status_string(12345) == "unknown status"
