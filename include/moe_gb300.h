@@ -68,9 +68,10 @@ size_t moe_capacity(int T, int K, int E, int align);
 
 /*
  * Bytes of scratch the layer needs: a 1 KB header (device error word), routing
- * chunk counters, the dW split schedule, the activation act [cap, I], the hidden
- * gradient [cap, 2I] (bf16 and fp16), the routed output gradient [cap, D] (bf16 and
- * fp16) and an fp16 copy of x_perm [cap, D].  One
+ * chunk counters, the dW split schedule, each routed slot's sorted row [T*K], the
+ * activation act [cap, I], the hidden gradient [cap, 2I] (bf16 and fp16), the routed
+ * output gradient [cap, D] (bf16 and fp16), an fp16 copy of x_perm [cap, D], fp16
+ * residuals of the weight-gradient operands and dA [cap, I] (fp16, with its residual).  One
  * workspace may serve the forward and the backward of the same sizes, but not
  * two calls running concurrently.  Returns 0 for invalid arguments.
  */

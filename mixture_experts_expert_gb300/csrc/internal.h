@@ -38,6 +38,7 @@ enum KernelId : int {
   kKRouterWGrad,
   kKRouterBwd,
   kKRouteFused,
+  kKBwdPrepPad,
   kNumKernelIds
 };
 
@@ -111,10 +112,11 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, con
 // Backward operand preparation for every sorted row s < offsets[E]:
 //   dy_perm[s] = dy[perm_src[s] / K] (bf16, unscaled), dy16[s] = fp16 of the same row,
 //   x16[s] = fp16(x[perm_src[s] / K]) (from x_perm[s] when x is null); zero rows on padding.
+// `inv` ([T*K] int32 scratch) receives each routed slot's sorted row (-1: none).
 cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
-                                 const int32_t* perm_src, const int32_t* offsets, int E, int K,
-                                 int D, int cap, uint16_t* dy_perm, uint16_t* dy16,
-                                 uint16_t* x16, cudaStream_t s);
+                                 const int32_t* perm_src, const int32_t* offsets, int T, int E,
+                                 int K, int D, int cap, int32_t* inv, uint16_t* dy_perm,
+                                 uint16_t* dy16, uint16_t* x16, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
                            int T, int K, int D, uint16_t* out, cudaStream_t s);

@@ -17,7 +17,7 @@ static const char* const kKernelNames[kNumKernelIds] = {
     "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
     "gemm_down",   "combine",    "bwd_prep_rows", "gemm_dA",    "gemm_bwd_gateup",
     "gemm_dx",     "dw_prep",    "gemm_dw_gateup", "gemm_dw_down", "router_topk",
-    "router_weight_grad", "router_backward", "route_permute"};
+    "router_weight_grad", "router_backward", "route_permute", "bwd_prep_pad"};
 
 const char* kernel_name(int id) {
   return (id >= 0 && id < kNumKernelIds) ? kKernelNames[id] : nullptr;
@@ -176,11 +176,12 @@ static size_t capacity_of(int T, int K, int E, int align) {
 static size_t up1k(size_t v) { return (v + 1023) & ~static_cast<size_t>(1023); }
 
 struct WsLayout {
-  size_t chunk_counts, dw_prefix, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, da, da_lo,
-      total;
+  size_t chunk_counts, dw_prefix, inv, act, dh, dyp, dh16, dyp16, xp16, act_lo, dh16_lo, da,
+      da_lo, total;
 };
 
-// header | routing chunk counters | dW split prefix | act | dH | dy_perm | dH fp16 |
+// header | routing chunk counters | dW split prefix | slot -> sorted row [T*K] (backward
+// row preparation) | act | dH | dy_perm | dH fp16 |
 // dy_perm fp16 | x_perm fp16 | w*act fp16 residual | dH fp16 residual (the residuals
 // are written only for experts whose weight gradient is split over several tiles) |
 // router-weighted dA fp16 | its fp16 residual (split experts only)
@@ -193,6 +194,8 @@ static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   o = up1k(o + static_cast<size_t>(E) * nch * 4);
   L.dw_prefix = o;
   o = up1k(o + static_cast<size_t>(E + 1) * 4);
+  L.inv = o;
+  o = up1k(o + static_cast<size_t>(T) * K * 4);
   L.act = o;
   o = up1k(o + cap * static_cast<size_t>(I) * 2);
   L.dh = o;
@@ -496,8 +499,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
 
   // 1. routed expert-output gradient rows (unscaled; the router weight is applied to dA in
   //    fp32) and the fp16 operand copies of the weight-gradient GEMMs
-  e = launch_bwd_prep_rows(dy, x, x_perm, perm_src, offsets, E, K, D, static_cast<int>(cap), dyp,
-                           dyp16, xp16, s);
+  e = launch_bwd_prep_rows(dy, x, x_perm, perm_src, offsets, T, E, K, D, static_cast<int>(cap),
+                           reinterpret_cast<int32_t*>(ws + L.inv), dyp, dyp16, xp16, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. dA = w * dy_perm W_d^T (scaled in fp32, kept in fp16), then the gate/up recompute

@@ -8,6 +8,13 @@ namespace moe {
 
 constexpr int kChunk = 256;           // flat routed slots per chunk (one warp each)
 constexpr int kRouteWarps = 8;        // warps per block in the count / scatter kernels
+constexpr int kPadSlices = 8;         // token-order copies: padding-zeroing blocks per expert
+
+__global__ void k_gather_tokens(const uint16_t* __restrict__ x,
+                                const int32_t* __restrict__ perm_src,
+                                const int32_t* __restrict__ inv,
+                                const int32_t* __restrict__ offsets, int T, int E, int K, int D,
+                                int token_blocks, uint16_t* __restrict__ x_perm);
 
 int route_num_chunks(int R) { return (R + kChunk - 1) / kChunk; }
 
@@ -335,8 +342,13 @@ cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, 
       e = cudaLaunchKernelEx(&cfg, k_route_fused, ids, w, R, E, align, nch, cap, chunk_counts,
                              counts, offsets, perm_src, inv_perm, w_perm, sync, err);
     }
-    if (e == cudaSuccess && x != nullptr)
-      e = launch_gather_rows(x, perm_src, nullptr, offsets, E, K, D, cap, x_perm, kKGatherX, s);
+    if (e == cudaSuccess && x != nullptr && R > 0) {
+      const int token_blocks = (R / K + 7) / 8;
+      LaunchScope ls(kKGatherX, s);
+      k_gather_tokens<<<token_blocks + E * kPadSlices, 256, 0, s>>>(
+          x, perm_src, inv_perm, offsets, R / K, E, K, D, token_blocks, x_perm);
+      e = cudaGetLastError();
+    }
     return e;
   }
   const int nchunks = route_num_chunks(R);
@@ -378,6 +390,80 @@ cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, 
 }
 
 // ------------------------------------------------------------------ row gather
+// Token-order copies: each routed token row is read once and written to its K sorted
+// rows; blocks past the token blocks zero the padding rows, kPadSlices blocks per expert.
+
+// [*lo, *end): the padding rows of expert e (its real rows come first in its segment).
+__device__ __forceinline__ void padding_rows(const int32_t* __restrict__ perm_src,
+                                             const int32_t* __restrict__ offsets, int e,
+                                             int* lo_out, int* end_out) {
+  int lo = __ldg(offsets + e), hi = __ldg(offsets + e + 1);
+  *end_out = hi;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(perm_src + mid) >= 0) lo = mid + 1; else hi = mid;
+  }
+  *lo_out = lo;
+}
+
+// Sorted row of slot j held by lane k = j - t*K of the warp of token t, or -1.  An entry
+// of a slot that reached no row (an expert id outside [0, E)) is stale, so it counts only
+// when perm_src points back at it.
+__device__ __forceinline__ int slot_row(const int32_t* __restrict__ inv,
+                                        const int32_t* __restrict__ perm_src, int rows, int t,
+                                        int K, int lane) {
+  if (lane >= K) return -1;
+  const int j = t * K + lane;
+  const int s = __ldg(inv + j);
+  return (s >= 0 && s < rows && __ldg(perm_src + s) == j) ? s : -1;
+}
+
+// x_perm[s] = x[t] for every sorted row s of token t; zero padding rows.
+__global__ void __launch_bounds__(256) k_gather_tokens(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ perm_src,
+    const int32_t* __restrict__ inv, const int32_t* __restrict__ offsets, int T, int E, int K,
+    int D, int token_blocks, uint16_t* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nvec = D >> 3;
+  if (static_cast<int>(blockIdx.x) >= token_blocks) {
+    const int b = blockIdx.x - token_blocks;
+    const int e = b / kPadSlices, slice = b - e * kPadSlices;
+    if (e >= E) return;
+    int lo, end;
+    padding_rows(perm_src, offsets, e, &lo, &end);
+    for (int r = lo + slice * (blockDim.x >> 5) + warp; r < end;
+         r += kPadSlices * (blockDim.x >> 5)) {
+      uint4* d = reinterpret_cast<uint4*>(x_perm) + static_cast<size_t>(r) * nvec;
+      for (int v = lane; v < nvec; v += 32) __stcs(d + v, make_uint4(0, 0, 0, 0));
+    }
+    return;
+  }
+  const int rows = __ldg(offsets + E);
+  const int wpg = (token_blocks * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += wpg) {
+    const int my_s = slot_row(inv, perm_src, rows, t, K, lane);
+    if (!__ballot_sync(0xffffffffu, my_s >= 0)) continue;
+    const uint4* sp = reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * D);
+    // warp-uniform trip count: every lane takes part in the shuffles of every step
+    for (int vb = 0; vb < nvec; vb += 32 * 8) {
+      const int v0 = vb + lane;
+      uint4 q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (v0 + 32 * u < nvec) q[u] = __ldg(sp + v0 + 32 * u);
+      for (int k = 0; k < K; ++k) {
+        const int s = __shfl_sync(0xffffffffu, my_s, k);
+        if (s < 0) continue;   // warp-uniform
+        uint4* d = reinterpret_cast<uint4*>(x_perm) + static_cast<size_t>(s) * nvec;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (v0 + 32 * u < nvec) __stcs(d + v0 + 32 * u, q[u]);
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint4 scale_bf16x8(uint4 q, float sc) {
   uint32_t* w = reinterpret_cast<uint32_t*>(&q);
 #pragma unroll
@@ -452,56 +538,115 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 q) {
   return q;
 }
 
-// For every sorted row s < offsets[E]: dy_perm[s] = dy[perm_src[s]/K] (bf16 copy),
-// dy16[s] = the same row in fp16, x16[s] = fp16(x_perm[s]); zero rows on padding.
+// Two kernels.  The first records each routed slot's sorted row (inv[j] = s).  A slot that
+// reached no row (an expert id outside [0, E)) keeps whatever its entry held, so the second
+// kernel accepts inv[j] = s only when perm_src[s] == j.  In the second, one warp per token reads the
+// token's dY and x rows once and writes them to its K sorted rows: dy_perm[s] = dy[t]
+// (bf16), dy16[s] = fp16(dy[t]), x16[s] = fp16(x[t]) (from the sorted copy of the row when
+// x is not given); its last E * kPadSlices blocks zero the three copies' padding rows.  In
+// sorted order the token rows would be re-read K times, mostly from DRAM once the copies
+// being written have pushed them out of L2.
+__global__ void __launch_bounds__(256) k_bwd_prep_pad(const int32_t* __restrict__ perm_src,
+                                                      const int32_t* __restrict__ offsets, int E,
+                                                      int32_t* __restrict__ inv) {
+  const int rows = __ldg(offsets + E);
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < rows; s += gridDim.x * blockDim.x) {
+    const int j = __ldg(perm_src + s);
+    if (j >= 0) inv[j] = s;
+  }
+}
+
 __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     const uint16_t* __restrict__ dy, const uint16_t* __restrict__ x,
-    const uint16_t* __restrict__ x_perm,
-    const int32_t* __restrict__ perm_src, const int32_t* __restrict__ offsets, int E, int K,
-    int D, uint16_t* __restrict__ dy_perm, uint16_t* __restrict__ dy16,
+    const uint16_t* __restrict__ x_perm, const int32_t* __restrict__ perm_src,
+    const int32_t* __restrict__ offsets, const int32_t* __restrict__ inv, int T, int E, int K,
+    int D, int token_blocks, uint16_t* __restrict__ dy_perm, uint16_t* __restrict__ dy16,
     uint16_t* __restrict__ x16) {
-  const int rows = __ldg(offsets + E);
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int nvec = D >> 3;
-  const int wpg = (gridDim.x * blockDim.x) >> 5;
-  for (int s = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; s < rows; s += wpg) {
-    const int j = __ldg(perm_src + s);
-    const size_t off = static_cast<size_t>(s) * D;
-    uint4* dp = reinterpret_cast<uint4*>(dy_perm + off);
-    uint4* d16 = reinterpret_cast<uint4*>(dy16 + off);
-    uint4* x16p = reinterpret_cast<uint4*>(x16 + off);
-    if (j < 0) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
+  if (static_cast<int>(blockIdx.x) >= token_blocks) {
+    // padding rows of expert e: its real rows come first in its segment
+    const int b = blockIdx.x - token_blocks;
+    const int e = b / kPadSlices, slice = b - e * kPadSlices;
+    if (e >= E) return;
+    int lo, end;
+    padding_rows(perm_src, offsets, e, &lo, &end);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int r = lo + slice * (blockDim.x >> 5) + warp; r < end;
+         r += kPadSlices * (blockDim.x >> 5)) {
+      const size_t off = static_cast<size_t>(r) * nvec;
+      uint4* dp = reinterpret_cast<uint4*>(dy_perm) + off;
+      uint4* d16 = reinterpret_cast<uint4*>(dy16) + off;
+      uint4* x16p = reinterpret_cast<uint4*>(x16) + off;
       for (int v = lane; v < nvec; v += 32) {
         __stcs(dp + v, z);
         __stcs(d16 + v, z);
         __stcs(x16p + v, z);
       }
-      continue;
     }
-    const size_t tok = static_cast<size_t>(j / K) * D;
-    const uint4* sp = reinterpret_cast<const uint4*>(dy + tok);
-    // the token's row of x (read K times, from cache) when given, else the sorted copy
-    const uint4* xp = reinterpret_cast<const uint4*>(x ? x + tok : x_perm + off);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 q = __ldg(sp + v);
-      const uint4 xq = __ldg(xp + v);
-      __stcs(dp + v, q);            // streaming stores: the dY / x rows stay cached
-      __stcs(d16 + v, bf16x8_to_f16x8(q));
-      __stcs(x16p + v, bf16x8_to_f16x8(xq));
+    return;
+  }
+  const int wpg = (token_blocks * blockDim.x) >> 5;
+  const int rows = __ldg(offsets + E);
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += wpg) {
+    const int my_s = slot_row(inv, perm_src, rows, t, K, lane);   // lane k: slot (t, k)
+    const unsigned valid = __ballot_sync(0xffffffffu, my_s >= 0);
+    if (!valid) continue;
+    const int s_first = __shfl_sync(0xffffffffu, my_s, __ffs(valid) - 1);
+    const uint4* sp = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(t) * D);
+    const uint4* xp = reinterpret_cast<const uint4*>(
+        x ? x + static_cast<size_t>(t) * D : x_perm + static_cast<size_t>(s_first) * D);
+    // warp-uniform trip count: every lane takes part in the shuffles of every step
+    for (int vb = 0; vb < nvec; vb += 32 * 4) {
+      const int v0 = vb + lane;
+      uint4 q[4], h[4], xh[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) {
+          q[u] = __ldg(sp + v);
+          xh[u] = bf16x8_to_f16x8(__ldg(xp + v));
+          h[u] = bf16x8_to_f16x8(q[u]);
+        }
+      }
+      for (int k = 0; k < K; ++k) {
+        const int s = __shfl_sync(0xffffffffu, my_s, k);
+        if (s < 0) continue;   // warp-uniform
+        const size_t off = static_cast<size_t>(s) * nvec;
+        uint4* dp = reinterpret_cast<uint4*>(dy_perm) + off;
+        uint4* d16 = reinterpret_cast<uint4*>(dy16) + off;
+        uint4* x16p = reinterpret_cast<uint4*>(x16) + off;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int v = v0 + 32 * u;
+          if (v < nvec) {
+            __stcs(dp + v, q[u]);   // streaming stores: written once, read by later kernels
+            __stcs(d16 + v, h[u]);
+            __stcs(x16p + v, xh[u]);
+          }
+        }
+      }
     }
   }
 }
 
 cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
-                                 const int32_t* perm_src, const int32_t* offsets, int E, int K,
-                                 int D, int cap, uint16_t* dy_perm, uint16_t* dy16,
-                                 uint16_t* x16, cudaStream_t s) {
-  int blocks = (cap + 7) / 8;
-  if (blocks < 1) blocks = 1;
+                                 const int32_t* perm_src, const int32_t* offsets, int T, int E,
+                                 int K, int D, int cap, int32_t* inv, uint16_t* dy_perm,
+                                 uint16_t* dy16, uint16_t* x16, cudaStream_t s) {
+  if (T > 0) {
+    int blocks = (cap + 255) / 256;
+    if (blocks > 1024) blocks = 1024;
+    LaunchScope ls(kKBwdPrepPad, s);
+    k_bwd_prep_pad<<<blocks, 256, 0, s>>>(perm_src, offsets, E, inv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int token_blocks = (T + 7) / 8;
   LaunchScope ls(kKBwdPrepRows, s);
-  k_bwd_prep_rows<<<blocks, 256, 0, s>>>(dy, x, x_perm, perm_src, offsets, E, K, D, dy_perm,
-                                         dy16, x16);
+  k_bwd_prep_rows<<<token_blocks + E * kPadSlices, 256, 0, s>>>(
+      dy, x, x_perm, perm_src, offsets, inv, T, E, K, D, token_blocks, dy_perm, dy16, x16);
   return cudaGetLastError();
 }
 

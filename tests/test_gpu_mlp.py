@@ -164,6 +164,25 @@ def test_backward_without_unsorted_x():
         assert torch.equal(a, b)
 
 
+def test_layer_without_tokens():
+    """T = 0: nothing is routed; Y and dX are empty and every weight gradient is exactly
+    zero (every expert is empty)."""
+    T, D, I, E, K = 0, 256, 128, 4, 2
+    g = {k: v.to(DEV) for k, v in random_layer(T, D, I, E, K, seed=30).items()}
+    layer = MoEExpertMLP(T, K, E, D, I, align=128, device=DEV)
+    layer.dw_gate.fill_(1.0)
+    layer.dw_up.fill_(1.0)
+    layer.dw_down.fill_(1.0)
+    y = layer.forward(g["x"], g["topk_ids"], g["topk_w"], g["w_gate"], g["w_up"], g["w_down"])
+    dx, dwg, dwu, dwd = layer.backward(g["dy"], g["w_gate"], g["w_up"], g["w_down"])
+    torch.cuda.synchronize()
+    assert layer.device_error()[0] == B.MOE_OK
+    assert y.shape == (0, D) and dx.shape == (0, D)
+    assert int(layer.offsets[-1]) == 0
+    for t in (dwg, dwu, dwd):
+        assert bool((t == 0).all())
+
+
 def test_split_expert_reduce_add():
     """One expert holds 5000 rows (> 2048): its weight gradient is split into three
     token chunks that are TMA reduce-added; the other experts are empty or small."""
@@ -184,7 +203,8 @@ def _sample_experts(counts, rng):
 
 
 @pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.sweep_shape(1024),
-                                   synth.sweep_shape(2048), synth.sweep_shape(32768),
+                                   synth.sweep_shape(2048), synth.sweep_shape(4096),
+                                   synth.sweep_shape(16384), synth.sweep_shape(32768),
                                    synth.sweep_shape(65536), synth.SKEWED, synth.SKEWED_STEEP,
                                    synth.LLAMA4_SCOUT, synth.SCOUT_SKEWED], ids=lambda s: s.name)
 def test_full_size_workloads_sampled(shape):
