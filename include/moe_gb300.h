@@ -152,9 +152,11 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *        dw_down[e] = sum_s (w act)_s^T dy_row_s,  dw_gate[e] = x_perm_e^T dG_e,
  *        dw_up[e] = x_perm_e^T dU_e
  *      computed from fp16 operands (x and dy convert exactly; the intermediates keep 10
- *      mantissa bits) with fp32 accumulation; experts with more than 4096 rows are split
- *      over several tiles whose parts are TMA reduce-added.  Experts with no rows get
- *      exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
+ *      mantissa bits) with fp32 accumulation; an expert with more than 4096 real rows
+ *      also runs the fp16 residuals of the rounded intermediates (compensated operands),
+ *      and one with more padded rows than the shape's dW chunk (moe_tuning_t, default
+ *      4096) is split over several tiles whose parts are TMA reduce-added.  Experts with
+ *      no rows get exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
  *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets/counts (counts may be NULL) from
  *   moe_route_permute, weights as in the forward -- all device.  x [T,D] bf16 (device) or
  *   NULL: the unsorted input of the forward; when given, step 4's fp16 copy of the sorted
@@ -283,8 +285,9 @@ typedef struct {
    * a shape with I % 256 != 0 runs as 128. */
   int da_tile_n;
   /* An expert with more padded rows than this has its weight gradient split into equal
-   * chunks of at most this many rows, reduce-added in fp32, with compensated fp16
-   * operands.  A multiple of 64 in [256, 65536]; default 4096. */
+   * chunks of at most this many rows, reduce-added in fp32.  A multiple of 64 in
+   * [256, 65536]; default 4096.  (Independently, an expert with more than 4096 real rows
+   * takes compensated value + residual fp16 operands in its weight gradients.) */
   int dw_chunk_rows;
 } moe_tuning_t;
 

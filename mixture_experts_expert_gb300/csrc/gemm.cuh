@@ -30,10 +30,10 @@
 //   GateUp  act[s, i]  = silu(x_perm[s] W_g[e])_i * (x_perm[s] W_u[e])_i   N: 128 gate + 128 up
 //   Down    y_perm[s]  = act[s] W_d[e]
 //   DA      dA[s]      = w_perm[s] * dy_perm[s] W_d[e]^T   (scaled in fp32, stored fp16; dy_perm
-//           unscaled); for experts split over several dW tiles also the fp16 residual
+//           unscaled); for experts with compensated dW operands also the fp16 residual
 //   BwdGU   recompute G, U as GateUp; the epilogue reads dA and writes w*act (fp16),
 //           dG = dA U silu'(G), dU = dA silu(G) (bf16 for Dx, fp16 for the dW GEMMs) and,
-//           for experts split over several dW tiles, the fp16 residuals v - fp16(v)
+//           for experts with compensated dW operands, the fp16 residuals v - fp16(v)
 //   Dx      dx_perm[s] = [dG dU][s] [W_g[e]; W_u[e]]^T                    (K = 2I)
 //   DwGU    [dW_g dW_u][e] = x16_e^T [dG dU]16_e        (K = the expert's token rows)
 //   DwD     dW_d[e]        = (w act)16_e^T dy16_e
@@ -41,8 +41,9 @@
 // are fp16 (10-bit mantissa; x and dY convert exactly) rather than bf16: the rounding of
 // the intermediates (dG, dU, w*act) is what bounds dW's absolute error.  dW tiles cover
 // at most dw_chunk_rows token rows; an expert with more rows is split into equal chunks on
-// tiles whose fp32 results are TMA reduce-added into a zeroed dW, and its rows run twice
-// (values, then residuals) so that its error does not grow with the row count.
+// tiles whose fp32 results are TMA reduce-added into a zeroed dW.  An expert with more
+// than kDwCompRows real rows runs its rows twice (values, then residuals), so that its
+// error stops growing with the row count.
 #pragma once
 
 #include "common.cuh"
@@ -99,11 +100,20 @@ struct TileInfo {
   int row0;     // dW: first token row of the K range
   int nkb;      // number of 64-deep K blocks
   int split;    // dW: the expert is split over several tiles (reduce-add)
-  int kb_half;  // dW of a split expert: K blocks per operand pass (values, then residuals)
+  int comp;     // dW: compensated operands (a value pass, then a residual pass)
+  int kb_half;  // dW of a compensated expert: K blocks per operand pass
   int ghost;    // pair kinds: this CTA's 128 rows lie past the expert's last row tile
   int swap;     // pair kinds: the expert's odd last row tile, computed transposed
   int tail_n;   // swap: token rows computed (a multiple of 32); the rest are padding
 };
+
+// Whether expert e's weight gradient takes compensated operands (see kDwCompRows): its real
+// rows when the counts are given, else its padded rows.
+__device__ __forceinline__ bool dw_compensated(const GemmParams& p, int e) {
+  const int rows =
+      p.counts ? __ldg(p.counts + e) : __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+  return rows > kDwCompRows;
+}
 
 // Largest e in [0, E) with arr[e] <= v (arr non-decreasing, arr[0] <= v < arr[E]).
 __device__ __forceinline__ int find_segment(const int* __restrict__ arr, int E, int v) {
@@ -184,6 +194,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, cons
                                                 int rank) {
   TileInfo ti;
   ti.split = 0;
+  ti.comp = 0;
   ti.row0 = 0;
   ti.kb_half = 0;
   ti.ghost = 0;
@@ -258,8 +269,9 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, cons
     rows = rows < per ? rows : per;
     ti.nkb = rows > 0 ? (rows + kBK - 1) / kBK : 0;
     ti.split = nch > 1;
+    ti.comp = dw_compensated(p, ti.e);
     ti.kb_half = ti.nkb;
-    if (ti.split) ti.nkb *= 2;   // compensated operands: the value pass, then the residual pass
+    if (ti.comp) ti.nkb *= 2;   // the value pass, then the residual pass
     const int mt = l / p.n_tiles;
     const int nt = l - mt * p.n_tiles;
     ti.m0 = mt * kBM;
@@ -298,7 +310,7 @@ __device__ __forceinline__ void issue_kblock(const GemmParams& p, const TileInfo
   } else {  // DwGU, DwD: both operands MN-major, K runs over token rows
     // a split expert runs its rows twice: with the fp16 values, then with the fp16
     // residuals of the rounded operand, into one accumulator
-    const bool lo = ti.split && kb >= ti.kb_half;
+    const bool lo = ti.comp && kb >= ti.kb_half;
     const int s0 = ti.row0 + (lo ? kb - ti.kb_half : kb) * kBK;
     const CUtensorMap* ma = (KIND == GemmKind::DwD && lo) ? &p.mapA1 : &p.mapA0;
     const CUtensorMap* mb = (KIND == GemmKind::DwGU && lo) ? &p.mapB1 : &p.mapB0;
@@ -626,7 +638,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
     return true;
   } else if constexpr (KIND == GemmKind::DA) {
     const int x = ti.n0 + 128 * rank + 32 * q;
-    const bool want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
+    const bool want_lo = dw_compensated(p, ti.e);
     for (int j = 0; j < nch; ++j) {
       const float wl = __ldg(p.w_perm + ti.m0 + 32 * j + lane);   // router weight of row lane
       uint32_t r[32];
@@ -684,7 +696,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
     const int f0 = ti.n0 + 64 * rank + 32 * pi;
     bool want_lo = false;
     if constexpr (KIND == GemmKind::BwdGU)
-      want_lo = (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
+      want_lo = dw_compensated(p, ti.e);
     for (int j = 0; j < nch; ++j) {
       const int row0 = ti.m0 + 32 * j;
       uint32_t g[32];
@@ -718,7 +730,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           d[i] = __half2float(__ushort_as_half(__ldg(da + static_cast<size_t>(i) * p.I)));
-        if (want_lo) {   // dA's fp16 residual, kept for the experts split over dW tiles
+        if (want_lo) {   // dA's fp16 residual, for experts with compensated dW operands
           const unsigned short* dl = reinterpret_cast<const unsigned short*>(p.dA_lo) +
                                      static_cast<size_t>(row0) * p.I + f0 + lane;
 #pragma unroll
@@ -895,7 +907,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
       } else if constexpr (KIND == GemmKind::DA) {
         const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
         const bool want_lo =
-            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
+            dw_compensated(p, ti.e);
         const int nch = p.tile_n / 32;
         for (int c = 0; c < nch; ++c) {
           uint32_t r[32];
@@ -912,7 +924,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
           uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
           stage_16_row(buf, lane, pk);
           store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
-          if (want_lo) {   // the fp16 residual, for experts split over dW tiles
+          if (want_lo) {   // the fp16 residual, for experts with compensated dW operands
             uint8_t* lb = ring_next<R16, 2048>(stg, ring, lane);
             stage_16_row(lb, lane, lo);
             store_box(&p.mapO1, lb, ti.n0 + 32 * c, row, lane, false);
@@ -921,9 +933,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
       } else if constexpr (KIND == GemmKind::BwdGU) {
         const int my_row = row + lane;
         const float wr = __ldg(p.w_perm + my_row);
-        // rows of an expert whose dW is split over several tiles also get the fp16 residuals
+        // rows of an expert with compensated dW operands also get the fp16 residuals
         const bool want_lo =
-            (__ldg(p.offsets + ti.e + 1) - __ldg(p.offsets + ti.e)) > p.dw_chunk_rows;
+            dw_compensated(p, ti.e);
         const uint4* da_row =
             reinterpret_cast<const uint4*>(p.dA + static_cast<size_t>(my_row) * p.I + ti.n0);
         const uint4* dl_row =

@@ -63,6 +63,11 @@ constexpr int kBK = 64;         // K per pipeline stage (one 128-byte swizzle ro
 // dW chunks of at most that many rows (reduce-added) and gets the compensated
 // (value + residual) fp16 operands.  The per-shape tuning may choose another multiple of 64.
 constexpr int kDwChunkRows = 4096;
+// Experts with more real rows than this take compensated (value + residual) fp16 operands
+// in their weight gradients: the error of one fp16 pass grows with the square root of the
+// rows summed, and above this count it would approach the tolerance.  Independent of the
+// chunking, which only spreads an expert's rows over more tiles.
+constexpr int kDwCompRows = 4096;
 constexpr int kMaxExperts = 1024;   // largest E the entry points accept
 
 struct GemmParams {
@@ -82,7 +87,7 @@ struct GemmParams {
   const int* dw_prefix;    // [E+1] dW split-K chunk prefix over experts (device), dW kinds only
   const float* w_perm;     // [cap] router weight per sorted row (DA, BwdGU)
   const uint16_t* dA;      // [cap, I] router-weighted dA, fp16 (BwdGU reads it)
-  const uint16_t* dA_lo;   // [cap, I] its fp16 residual (rows of experts split over dW tiles)
+  const uint16_t* dA_lo;   // [cap, I] its fp16 residual (rows of compensated experts)
   int* err;                // device error word
   int E, D, I;
   int n_tiles;             // N tiles per M tile

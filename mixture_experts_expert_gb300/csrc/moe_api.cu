@@ -183,8 +183,8 @@ struct WsLayout {
 // header | routing chunk counters | dW split prefix | slot -> sorted row [T*K] (backward
 // row preparation) | act | dH | dy_perm | dH fp16 |
 // dy_perm fp16 | x_perm fp16 | w*act fp16 residual | dH fp16 residual (the residuals
-// are written only for experts whose weight gradient is split over several tiles) |
-// router-weighted dA fp16 | its fp16 residual (split experts only)
+// are written only for experts whose weight gradient takes compensated operands) |
+// router-weighted dA fp16 | its fp16 residual (those experts only)
 static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   WsLayout L;
   const size_t cap = capacity_of(T, K, E, align);

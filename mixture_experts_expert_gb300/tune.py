@@ -12,8 +12,7 @@ from the defaults:
    each GEMM's own time decides;
 2. transposed odd tail tiles on or off: the token-row GEMMs' summed time;
 3. the dA GEMM's tile width (256 or 128 columns): its own time;
-4. the dW chunk rows (at most 4096): dW preparation + dA + backward gate/up + both dW
-   GEMMs.
+4. the dW chunk rows: dW preparation + dA + backward gate/up + both dW GEMMs.
 
 Workloads with the same (T, K, E, D, I) share one table entry; their times are summed,
 so an entry serves a uniform and a skewed routing of that size alike.  The choices
@@ -32,14 +31,13 @@ import sys
 KIND_OF_GEMM = {"gate_up": "gemm_gateup_swiglu", "down": "gemm_down", "dA": "gemm_dA",
                 "bwd_gate_up": "gemm_bwd_gateup", "dx": "gemm_dx"}
 DW_KERNELS = ("dw_prep", "gemm_dA", "gemm_bwd_gateup", "gemm_dw_gateup", "gemm_dw_down")
-# Larger chunks run faster on skewed routings (no zeroing, reduce-add or compensating
-# pass for their hot experts) but leave up to that many rows in one uncompensated fp16
-# pass, whose error grows with the row count: 4096 is the most the accuracy bound allows.
-CHUNK_CANDIDATES = (1024, 2048, 4096)
+# The chunk only spreads an expert's rows over tiles (whether its operands are
+# compensated depends on its row count alone), so every candidate is equally accurate.
+CHUNK_CANDIDATES = (1024, 2048, 4096, 8192, 16384)
 DEFAULT_WORKLOADS = ("tiny", "qwen3_30b_a3b_T1024", "qwen3_30b_a3b_T2048",
                      "qwen3_30b_a3b_T4096", "qwen3_30b_a3b", "qwen3_30b_a3b_T16384",
                      "skewed_zipf1.2", "skewed_zipf1.4", "qwen3_30b_a3b_T32768",
-                     "llama4_scout", "llama4_scout_zipf1.2")
+                     "qwen3_30b_a3b_T65536", "llama4_scout", "llama4_scout_zipf1.2")
 TABLE_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "csrc",
                           "tuning_table.inc")
 

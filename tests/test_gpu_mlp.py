@@ -183,9 +183,21 @@ def test_layer_without_tokens():
         assert bool((t == 0).all())
 
 
+def test_compensated_expert():
+    """One expert holds 7000 rows (more than 4096): its weight gradients take the
+    compensated operands (a value pass and a residual pass) and are split into two
+    4096-row chunks that are TMA reduce-added."""
+    T, D, I, E, K = 7300, 256, 128, 4, 1
+    ids = torch.full((T, K), 1, dtype=torch.int32)
+    ids[:200, 0] = 0
+    ids[200:300, 0] = 3
+    check_full(random_layer(T, D, I, E, K, seed=31, ids=ids), T, D, I, E, K)
+
+
 def test_split_expert_reduce_add():
-    """One expert holds 5000 rows (> 2048): its weight gradient is split into three
-    token chunks that are TMA reduce-added; the other experts are empty or small."""
+    """One expert holds 5000 rows (> 4096): its weight gradient is split into two
+    token chunks that are TMA reduce-added, with compensation (5000 > 4096); the
+    other experts are empty or small."""
     T, D, I, E, K = 5200, 256, 128, 4, 1
     ids = torch.full((T, K), 2, dtype=torch.int32)
     ids[:150, 0] = 0

@@ -63,6 +63,16 @@ def test_choices_match_oracle(ch):
     with_choices(ch, lambda: check_full(inp, T, D, I, E, K))
 
 
+def test_compensated_expert_unsplit():
+    """A 7000-row expert with 16384-row chunks: compensated operands in one chunk (no
+    reduce-add)."""
+    T, D, I, E, K = 7300, 256, 128, 3, 1
+    ids = torch.full((T, K), 2, dtype=torch.int32)
+    ids[:300, 0] = 0
+    inp = random_layer(T, D, I, E, K, seed=23, ids=ids)
+    with_choices(choices(dw_chunk_rows=16384), lambda: check_full(inp, T, D, I, E, K))
+
+
 def test_tile_order_changes_no_bit():
     ids, T, E = skewed_ids(seed=6)
     inp = random_layer(T, D, I, E, K, seed=22, ids=ids)
