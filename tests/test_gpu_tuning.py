@@ -85,3 +85,15 @@ def test_tile_order_changes_no_bit():
                                          layer.dw_down)])
     for a, b in zip(*outs):
         assert torch.equal(a, b)
+
+
+def test_tuner_runs_on_the_tiny_layer(capsys, tmp_path):
+    """The tuner measures every choice on a workload and prints a table the library can
+    compile (it leaves no override behind)."""
+    out = tmp_path / "t.json"
+    tune.main(["--workloads", "tiny", "--steps", "2", "--warmup", "1", "--reps", "1",
+               "--json", str(out)])
+    text = capsys.readouterr().out
+    assert "{256, 2, 8, 256, 128, {" in text and text.rstrip().endswith("1, 256, 4096},")
+    assert B.moe_tuning_get(256, 2, 8, 256, 128)[1] != "override"
+    assert out.exists()
