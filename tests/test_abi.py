@@ -29,6 +29,20 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(exported) == names
 
 
+def test_host_entry_points_from_plain_c(lib, tmp_path):
+    """The header compiles as C99 and the host-only calls work from a C program."""
+    import os
+    here = os.path.dirname(os.path.abspath(__file__))
+    exe = tmp_path / "abi_from_c"
+    inc = os.path.join(os.path.dirname(here), "include")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc,
+                    os.path.join(here, "abi_from_c.c"), B.LIB_PATH,
+                    "-Wl,-rpath," + os.path.dirname(B.LIB_PATH), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "FAIL" not in out.stdout and out.stdout.count("ok ") >= 12
+
+
 def test_library_is_sm103a_only():
     assert "arch=compute_103a,code=sm_103a" in " ".join(Bld.ARCH)
 
