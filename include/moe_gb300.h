@@ -48,7 +48,10 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = -2,   /* not an sm_103 device, or a shape the kernels do not cover */
   MOE_ERR_CUDA = -3,          /* a CUDA runtime / driver call failed */
   MOE_ERR_DEVICE_TIMEOUT = -4,/* (device error word) a kernel's bounded wait gave up */
-  MOE_ERR_BAD_INDEX = -5      /* (device error word) an expert id outside [0, E) */
+  MOE_ERR_BAD_INDEX = -5,     /* (device error word) an expert id outside [0, E) */
+  MOE_ERR_FP16_RANGE = -6     /* (device error word) moe_expert_mlp_bwd met an x or dy value
+                                 of magnitude >= 65536 (or inf / NaN), which its fp16
+                                 weight-gradient operands cannot hold */
 } moe_status_t;
 
 /* Version of this ABI (MOE_ABI_VERSION). */
@@ -156,7 +159,10 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *      also runs the fp16 residuals of the rounded intermediates (compensated operands),
  *      and one with more padded rows than the shape's dW chunk (moe_tuning_t, default
  *      4096) is split over several tiles whose parts are TMA reduce-added.  Experts with
- *      no rows get exactly zero.  x, dy and the intermediates must stay within the fp16 range (|v| < 65504).
+ *      no rows get exactly zero.  x, dy and the intermediates must stay within the fp16
+ *      range (|v| < 65504): an x or dy value outside it is reported in the device error
+ *      word as MOE_ERR_FP16_RANGE (the results of that call are then not meaningful); the
+ *      intermediates are not checked.
  *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets/counts (counts may be NULL) from
  *   moe_route_permute, weights as in the forward -- all device.  x [T,D] bf16 (device) or
  *   NULL: the unsorted input of the forward; when given, step 4's fp16 copy of the sorted
@@ -247,8 +253,8 @@ int moe_route_permute_noalloc(const int32_t* topk_ids, const float* topk_w,
 
 /*
  * Reads and clears the device error word of `workspace` (synchronises `stream`).
- * *code receives MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_DEVICE_TIMEOUT; *detail the
- * raw device code (which role timed out).  After an error it also zeroes the rest of the
+ * *code receives MOE_OK, MOE_ERR_BAD_INDEX, MOE_ERR_FP16_RANGE or MOE_ERR_DEVICE_TIMEOUT;
+ * *detail the raw device code (which role timed out).  After an error it also zeroes the rest of the
  * workspace header (counters a kernel that gave up may leave set): call it, or
  * moe_workspace_init, before reusing a workspace after an error.  For tests and debugging.
  */

@@ -24,6 +24,7 @@ MOE_ERR_UNSUPPORTED = -2
 MOE_ERR_CUDA = -3
 MOE_ERR_DEVICE_TIMEOUT = -4
 MOE_ERR_BAD_INDEX = -5
+MOE_ERR_FP16_RANGE = -6
 
 
 class MoEError(RuntimeError):

@@ -16,6 +16,7 @@ enum DevErr : int {
   kDevTimeoutMma = 3,       // MMA issuer gave up waiting on data or TMEM
   kDevTimeoutEpilogue = 4,  // epilogue gave up waiting on an accumulator
   kDevTimeoutRoute = 6,     // the fused routing kernel gave up at a grid barrier
+  kDevFp16Range = 7,        // an x or dY value outside the fp16 range (the dW operands)
 };
 
 // Identifiers of every kernel the library launches (for launch counting and timing).
@@ -121,7 +122,7 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, con
 cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
                                  const int32_t* perm_src, const int32_t* offsets, int T, int E,
                                  int K, int D, int cap, int32_t* inv, uint16_t* dy_perm,
-                                 uint16_t* dy16, uint16_t* x16, cudaStream_t s);
+                                 uint16_t* dy16, uint16_t* x16, int* err, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
                            int T, int K, int D, uint16_t* out, cudaStream_t s);

@@ -324,6 +324,7 @@ MOE_EXPORT const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case MOE_ERR_BAD_INDEX: return "expert id out of range";
+    case MOE_ERR_FP16_RANGE: return "x or dY value outside the fp16 range";
     default: return "unknown status";
   }
 }
@@ -500,7 +501,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   // 1. routed expert-output gradient rows (unscaled; the router weight is applied to dA in
   //    fp32) and the fp16 operand copies of the weight-gradient GEMMs
   e = launch_bwd_prep_rows(dy, x, x_perm, perm_src, offsets, T, E, K, D, static_cast<int>(cap),
-                           reinterpret_cast<int32_t*>(ws + L.inv), dyp, dyp16, xp16, s);
+                           reinterpret_cast<int32_t*>(ws + L.inv), dyp, dyp16, xp16, err, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. dA = w * dy_perm W_d^T (scaled in fp32, kept in fp16), then the gate/up recompute
@@ -673,6 +674,7 @@ MOE_EXPORT int moe_get_device_error(void* workspace, int* code, int* detail, voi
   if (detail) *detail = raw;
   if (raw == kDevOk) *code = MOE_OK;
   else if (raw == kDevBadExpertId) *code = MOE_ERR_BAD_INDEX;
+  else if (raw == kDevFp16Range) *code = MOE_ERR_FP16_RANGE;
   else *code = MOE_ERR_DEVICE_TIMEOUT;
   if (raw != 0) {
     // clears the word and the header's barrier counters a kernel that gave up may leave set

@@ -538,6 +538,17 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 q) {
   return q;
 }
 
+// Bit 15 of each 16-bit half set where the bf16 value's magnitude is at least 65536 (or
+// it is inf / NaN): values the fp16 copies of the weight-gradient operands cannot hold
+// (fp16 tops out at 65504; the largest bf16 below 65536 is 65280).
+__device__ __forceinline__ uint32_t fp16_overflow_bits(uint4 q) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&q);
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r |= (w[i] & 0x7fff7fffu) + 0x38803880u;   // 0x4780 + 0x3880 = 0x8000
+  return r & 0x80008000u;
+}
+
 // Two kernels.  The first records each routed slot's sorted row (inv[j] = s).  A slot that
 // reached no row (an expert id outside [0, E)) keeps whatever its entry held, so the second
 // kernel accepts inv[j] = s only when perm_src[s] == j.  In the second, one warp per token reads the
@@ -561,7 +572,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     const uint16_t* __restrict__ x_perm, const int32_t* __restrict__ perm_src,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ inv, int T, int E, int K,
     int D, int token_blocks, uint16_t* __restrict__ dy_perm, uint16_t* __restrict__ dy16,
-    uint16_t* __restrict__ x16) {
+    uint16_t* __restrict__ x16, int* err) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nvec = D >> 3;
@@ -597,6 +608,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     const uint4* sp = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(t) * D);
     const uint4* xp = reinterpret_cast<const uint4*>(
         x ? x + static_cast<size_t>(t) * D : x_perm + static_cast<size_t>(s_first) * D);
+    uint32_t big = 0;   // bit 15 of a half set: a bf16 value the fp16 copies cannot hold
     // warp-uniform trip count: every lane takes part in the shuffles of every step
     for (int vb = 0; vb < nvec; vb += 32 * 4) {
       const int v0 = vb + lane;
@@ -606,7 +618,9 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
         const int v = v0 + 32 * u;
         if (v < nvec) {
           q[u] = __ldg(sp + v);
-          xh[u] = bf16x8_to_f16x8(__ldg(xp + v));
+          const uint4 xq = __ldg(xp + v);
+          big |= fp16_overflow_bits(q[u]) | fp16_overflow_bits(xq);
+          xh[u] = bf16x8_to_f16x8(xq);
           h[u] = bf16x8_to_f16x8(q[u]);
         }
       }
@@ -628,13 +642,14 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
         }
       }
     }
+    if (__any_sync(0xffffffffu, big != 0) && lane == 0) report_error(err, kDevFp16Range);
   }
 }
 
 cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
                                  const int32_t* perm_src, const int32_t* offsets, int T, int E,
                                  int K, int D, int cap, int32_t* inv, uint16_t* dy_perm,
-                                 uint16_t* dy16, uint16_t* x16, cudaStream_t s) {
+                                 uint16_t* dy16, uint16_t* x16, int* err, cudaStream_t s) {
   if (T > 0) {
     int blocks = (cap + 255) / 256;
     if (blocks > 1024) blocks = 1024;
@@ -646,7 +661,8 @@ cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const ui
   const int token_blocks = (T + 7) / 8;
   LaunchScope ls(kKBwdPrepRows, s);
   k_bwd_prep_rows<<<token_blocks + E * kPadSlices, 256, 0, s>>>(
-      dy, x, x_perm, perm_src, offsets, inv, T, E, K, D, token_blocks, dy_perm, dy16, x16);
+      dy, x, x_perm, perm_src, offsets, inv, T, E, K, D, token_blocks, dy_perm, dy16, x16,
+      err);
   return cudaGetLastError();
 }
 
