@@ -1,6 +1,7 @@
 // Routing and data-movement kernels (HBM-bound): expert histogram, prefix scan,
-// stable scatter into expert-sorted order, row gather (x and the router-weighted
-// dY), the weighted combine back to tokens, and the dW split-K preparation.
+// stable scatter into expert-sorted order, the token-order copies into sorted rows
+// (x for the forward; dY and the fp16 dW operands for the backward), the weighted
+// combine back to tokens, and the dW split-K preparation.
 #include "common.cuh"
 #include "internal.h"
 
