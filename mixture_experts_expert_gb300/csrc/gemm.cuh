@@ -552,6 +552,37 @@ __device__ __forceinline__ void store_box(const CUtensorMap* map, const uint8_t*
   __syncwarp();
 }
 
+// Group staging: before staging N boxes into the next N slots of an NBUF-slot ring, at
+// most NBUF - N earlier stores may still be reading theirs (those used other slots).
+template <int NBUF, int N>
+__device__ __forceinline__ void ring_reserve(int lane) {
+  static_assert(N <= NBUF, "group larger than the ring");
+  if (lane == 0) bulk_wait_read<NBUF - N>();
+  __syncwarp();
+}
+template <int NBUF, int BYTES>
+__device__ __forceinline__ uint8_t* ring_slot(uint8_t* base, int& ring) {
+  uint8_t* b = base + (ring % NBUF) * BYTES;
+  ++ring;
+  return b;
+}
+
+// Hands a staged box to TMA without a fence of its own: the caller fences once (all
+// lanes, then __syncwarp) for every box it staged before issuing them.
+__device__ __forceinline__ void issue_box(const CUtensorMap* map, const uint8_t* buf, int x,
+                                          int y, int lane) {
+  if (lane == 0) {
+    tma_store_2d(map, buf, x, y);
+    bulk_commit();
+  }
+}
+
+// One proxy fence for a group of staged boxes.
+__device__ __forceinline__ void fence_boxes() {
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // fp16 residuals (v0 - fp16(v0), v1 - fp16(v1)) given the packed fp16 pair.
 __device__ __forceinline__ uint32_t f16x2_residual(uint32_t packed, float v0, float v1) {
   const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&packed));
@@ -997,31 +1028,41 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
             lu[i] = f16x2_residual(pu16[i], r[0][2], r[1][2]);
           }
           const int col = ti.n0 + 32 * c;
-          uint8_t* b0 = ring_next<R16, 2048>(stg, ring, lane);
+          // boxes are staged in groups of up to R16 (the ring) and fenced once per group
+          ring_reserve<R16, 3>(lane);
+          uint8_t* b0 = ring_slot<R16, 2048>(stg, ring);
           stage_16_row(b0, lane, pa);
-          store_box(&p.mapO0, b0, col, row, lane, false);        // w*act, fp16
-          uint8_t* b1 = ring_next<R16, 2048>(stg, ring, lane);
+          uint8_t* b1 = ring_slot<R16, 2048>(stg, ring);
           stage_16_row(b1, lane, pg);
-          store_box(&p.mapO1, b1, col, row, lane, false);        // dG, bf16
-          uint8_t* b2 = ring_next<R16, 2048>(stg, ring, lane);
+          uint8_t* b2 = ring_slot<R16, 2048>(stg, ring);
           stage_16_row(b2, lane, pu);
-          store_box(&p.mapO1, b2, p.I + col, row, lane, false);  // dU, bf16
-          uint8_t* b3 = ring_next<R16, 2048>(stg, ring, lane);
+          fence_boxes();
+          issue_box(&p.mapO0, b0, col, row, lane);        // w*act, fp16
+          issue_box(&p.mapO1, b1, col, row, lane);        // dG, bf16
+          issue_box(&p.mapO1, b2, p.I + col, row, lane);  // dU, bf16
+          __syncwarp();
+          ring_reserve<R16, 2>(lane);
+          uint8_t* b3 = ring_slot<R16, 2048>(stg, ring);
           stage_16_row(b3, lane, pg16);
-          store_box(&p.mapO2, b3, col, row, lane, false);        // dG, fp16
-          uint8_t* b4 = ring_next<R16, 2048>(stg, ring, lane);
+          uint8_t* b4 = ring_slot<R16, 2048>(stg, ring);
           stage_16_row(b4, lane, pu16);
-          store_box(&p.mapO2, b4, p.I + col, row, lane, false);  // dU, fp16
+          fence_boxes();
+          issue_box(&p.mapO2, b3, col, row, lane);        // dG, fp16
+          issue_box(&p.mapO2, b4, p.I + col, row, lane);  // dU, fp16
+          __syncwarp();
           if (want_lo) {
-            uint8_t* c0 = ring_next<R16, 2048>(stg, ring, lane);
+            ring_reserve<R16, 3>(lane);
+            uint8_t* c0 = ring_slot<R16, 2048>(stg, ring);
             stage_16_row(c0, lane, la);
-            store_box(&p.mapO3, c0, col, row, lane, false);        // w*act residual
-            uint8_t* c1 = ring_next<R16, 2048>(stg, ring, lane);
+            uint8_t* c1 = ring_slot<R16, 2048>(stg, ring);
             stage_16_row(c1, lane, lg);
-            store_box(&p.mapO4, c1, col, row, lane, false);        // dG residual
-            uint8_t* c2 = ring_next<R16, 2048>(stg, ring, lane);
+            uint8_t* c2 = ring_slot<R16, 2048>(stg, ring);
             stage_16_row(c2, lane, lu);
-            store_box(&p.mapO4, c2, p.I + col, row, lane, false);  // dU residual
+            fence_boxes();
+            issue_box(&p.mapO3, c0, col, row, lane);        // w*act residual
+            issue_box(&p.mapO4, c1, col, row, lane);        // dG residual
+            issue_box(&p.mapO4, c2, p.I + col, row, lane);  // dU residual
+            __syncwarp();
           }
         }
       } else {  // DwGU, DwD: fp32 out, plain store or split-K reduce-add
