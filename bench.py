@@ -167,85 +167,123 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(shape, budget_s=12.0):
-    """The oracle as it stands, on this host's cores, over a bounded sample: the
-    forward and backward of the first experts of the workload, expert by expert,
-    until the time budget is spent."""
-    import numpy as np
-    import torch
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the architecture)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
 
-    import oracle
-    from mixture_experts_expert_gb300 import synth
-    s = shape
-    inp = synth.make_inputs(s)
-    x = inp["x"].double().numpy()
-    dy = inp["dy"].double().numpy()
-    ids = inp["topk_ids"].numpy().astype(np.int64)
-    w = inp["topk_w"].double().numpy()
-    r = oracle.route_permute(ids, w, x, s.E, 128)
-    wg = [inp["w_gate"][e].double().numpy() for e in range(s.E)]
-    wu = [inp["w_up"][e].double().numpy() for e in range(s.E)]
-    wd = [inp["w_down"][e].double().numpy() for e in range(s.E)]
-    done, rows, t0 = [], 0, time.perf_counter()
-    for e in range(s.E):
-        oracle.expert_mlp_fwd(r["x_perm"], wg, wu, wd, r["offsets"], experts=[e])
-        oracle.expert_mlp_bwd(dy, r["x_perm"], r["perm_src"], r["w_perm"], r["offsets"],
-                              wg, wu, wd, s.K, experts=[e])
+
+def workload_config(s, world=1):
+    """The `config` object of every line this script prints for workload `s`."""
+    return {"workload": s.name, "T": s.T, "D": s.D, "I": s.I, "E": s.E, "K": s.K,
+            "align": 128, "router": s.router,
+            "l2": "working set larger than L2 (expert weights alone 3*E*D*I*2 bytes)",
+            "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"}
+
+
+class OracleSample:
+    """The oracle as it stands, on this host's cores, expert by expert: the workload's
+    inputs and sorted rows are prepared once; run(e) times the forward and the backward of
+    expert e, each on its own."""
+
+    def __init__(self, shape):
+        import numpy as np
+
+        import oracle
+        from mixture_experts_expert_gb300 import synth
+        self.s = s = shape
+        self.oracle = oracle
+        inp = synth.make_inputs(s)
+        x = inp["x"].double().numpy()
+        self.dy = inp["dy"].double().numpy()
+        ids = inp["topk_ids"].numpy().astype(np.int64)
+        w = inp["topk_w"].double().numpy()
+        self.r = oracle.route_permute(ids, w, x, s.E, 128)
+        self.wg, self.wu, self.wd = ([t[e].double().numpy() for e in range(s.E)]
+                                     for t in (inp["w_gate"], inp["w_up"], inp["w_down"]))
+
+    def run(self, e):
+        """(routed rows of expert e, forward seconds, backward seconds)."""
+        o, r = self.oracle, self.r
+        t0 = time.perf_counter()
+        o.expert_mlp_fwd(r["x_perm"], self.wg, self.wu, self.wd, r["offsets"], experts=[e])
+        t1 = time.perf_counter()
+        o.expert_mlp_bwd(self.dy, r["x_perm"], r["perm_src"], r["w_perm"], r["offsets"],
+                         self.wg, self.wu, self.wd, self.s.K, experts=[e])
+        t2 = time.perf_counter()
+        return int(r["counts"][e]), t1 - t0, t2 - t1
+
+
+def cpu_baseline(shape, budget_s=12.0, router=None):
+    """The oracle timed on this host's cores over a bounded sample of the workload, forward
+    and backward separately (FLOPs counted as for the GPU: 6 and 12 R*D*I).  With
+    `router` = (logits, ids) (host arrays: the logits the router kernel was given and the
+    ids it chose) the leg also checks that choice against the oracle's router."""
+    smp = OracleSample(shape)
+    rows, t_f, t_b, done = 0, 0.0, 0.0, []
+    for e in range(shape.E):
+        r_e, f_e, b_e = smp.run(e)
+        rows, t_f, t_b = rows + r_e, t_f + f_e, t_b + b_e
         done.append(e)
-        rows += int(r["counts"][e])
-        if time.perf_counter() - t0 > budget_s:
+        if t_f + t_b > budget_s:
             break
-    dt = time.perf_counter() - t0
-    flops = 18.0 * rows * s.D * s.I
-    del torch
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"fp64 forward+backward of experts 0..{done[-1]} ({rows} routed rows of "
-                      f"{s.R}) of the {s.name} layer, {dt:.1f} s"}
+    s = shape
+    rdi = rows * s.D * s.I
+    out = {"value": 18.0 * rdi / (t_f + t_b) / 1e12, "unit": "TFLOP/s",
+           "fwd": 6.0 * rdi / t_f / 1e12, "bwd": 12.0 * rdi / t_b / 1e12,
+           "cores": os.cpu_count(), "cpu_model": cpu_model(), "kind": "oracle",
+           "sample": f"fp64 forward and backward of experts {done[0]}..{done[-1]} ({rows} "
+                     f"routed rows of {s.R}) of the {s.name} layer, {t_f:.1f} s forward + "
+                     f"{t_b:.1f} s backward"}
+    if router is not None:
+        import numpy as np
+        logits, ids = router
+        ids_ref, _ = smp.oracle.router_topk(logits, s.K, s.router)
+        out["router_choice_matches_oracle"] = bool(np.array_equal(ids, ids_ref))
+    return out
 
 
 def run_reference(args, shape):
-    """The CPU oracle as the reference arm: each step is a bounded sample (one
-    expert's forward and backward), timed on the host cores."""
-    import numpy as np
-
-    import oracle
-    from mixture_experts_expert_gb300 import synth
+    """The CPU oracle as the reference arm: each step is a bounded sample (one expert's
+    forward and backward), timed on the host cores."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     s = shape
-    inp = synth.make_inputs(s)
-    x = inp["x"].double().numpy()
-    dy = inp["dy"].double().numpy()
-    ids = inp["topk_ids"].numpy().astype(np.int64)
-    w = inp["topk_w"].double().numpy()
-    r = oracle.route_permute(ids, w, x, s.E, 128)
-    wg, wu, wd = (inp[k] for k in ("w_gate", "w_up", "w_down"))
-    lists = [[t[e].double().numpy() for e in range(s.E)] for t in (wg, wu, wd)]
-
-    def step(e):
-        oracle.expert_mlp_fwd(r["x_perm"], *lists, r["offsets"], experts=[e])
-        oracle.expert_mlp_bwd(dy, r["x_perm"], r["perm_src"], r["w_perm"], r["offsets"], *lists,
-                              s.K, experts=[e])
-        return int(r["counts"][e])
-
+    smp = OracleSample(s)
     for i in range(args.warmup):
-        step(i % s.E)
-    rows, t0 = 0, time.perf_counter()
+        smp.run(i % s.E)
+    rows, t_f, t_b = 0, 0.0, 0.0
     for i in range(args.steps):
-        rows += step((args.warmup + i) % s.E)
-    dt = time.perf_counter() - t0
-    value = 18.0 * rows * s.D * s.I / dt / 1e12
-    sample = (f"fp64 forward+backward of one expert per step ({rows} routed rows in "
+        r_i, f_i, b_i = smp.run((args.warmup + i) % s.E)
+        rows, t_f, t_b = rows + r_i, t_f + f_i, t_b + b_i
+    dt = t_f + t_b
+    rdi = rows * s.D * s.I
+    value = 18.0 * rdi / dt / 1e12
+    sample = (f"fp64 forward and backward of one expert per step ({rows} routed rows in "
               f"{args.steps} steps) of the {s.name} layer")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": s.name, "T": s.T, "D": s.D, "I": s.I, "E": s.E, "K": s.K},
+            "config": workload_config(s, args.gpus),
+            "fwd_tflops": 6.0 * rdi / t_f / 1e12, "bwd_tflops": 12.0 * rdi / t_b / 1e12,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
-                             "kind": "oracle", "sample": sample},
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -276,8 +314,11 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    build_status = None
     if rank == 0 or world == 1:
         Bld.build()
+        build_status = Bld.last_status
+        print(f"libmoe_gb300: {build_status} {Bld.LIB_PATH}", file=sys.stderr, flush=True)
     if world > 1:
         dist.barrier()
     B.lib()
@@ -455,8 +496,7 @@ def main():
     torch.cuda.synchronize()
     B.moe_timing_enable(False)
     router_ms = {k: v[0] / v[1] for k, v in B.moe_timing_collect().items()}
-    # the routing the kernel chose is the routing the inputs were generated with
-    routed_same = bool(torch.equal(layer.topk_ids, inp["topk_ids"]))
+    router_choice = (logits.cpu().numpy(), layer.topk_ids.cpu().numpy())
 
     # ---------------- roofline of the dominant kernel (largest share of the step)
     peaks, peak_src = load_peaks()
@@ -516,10 +556,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": s.name, "T": s.T, "D": s.D, "I": s.I, "E": s.E, "K": s.K,
-                   "align": 128, "router": s.router,
-                   "l2": "working set larger than L2 (expert weights alone 3*E*D*I*2 bytes)",
-                   "parallelism": f"{world} independent replicas" if world > 1 else "single GPU"},
+        "config": workload_config(s, world),
         "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
         "fwd_frac_of_peak": fwd_tflops / peak_tf, "bwd_frac_of_peak": bwd_tflops / peak_tf,
         "peak_bf16_tflops": peak_tf, "peak_source": peak_src,
@@ -552,15 +589,18 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clocks,
-        "router": {"ms_per_launch": router_ms, "same_routing_as_inputs": routed_same,
+        "router": {"ms_per_launch": router_ms,
                    "weight_grad_gbs": (s.R * s.D * 2 + s.T * s.D * 2) /
                                       (router_ms.get("router_weight_grad", float("nan")) * 1e-3) / 1e9,
                    "note": "router step, outside the expert-MLP metric"},
     }
     tun, tun_src = B.moe_tuning_get(s.T, s.K, s.E, s.D, s.I)
     line["tuning"] = {"source": tun_src, **tun}
+    line["build"] = build_status   # "compiled" on this host, or "reused" (source hash matched)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(s)
+        line["cpu_baseline"] = cpu_baseline(s, router=router_choice)
+        line["router"]["choice_matches_oracle"] = line["cpu_baseline"].pop(
+            "router_choice_matches_oracle")
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -49,9 +49,9 @@ typedef enum {
   MOE_ERR_CUDA = -3,          /* a CUDA runtime / driver call failed */
   MOE_ERR_DEVICE_TIMEOUT = -4,/* (device error word) a kernel's bounded wait gave up */
   MOE_ERR_BAD_INDEX = -5,     /* (device error word) an expert id outside [0, E) */
-  MOE_ERR_FP16_RANGE = -6     /* (device error word) moe_expert_mlp_bwd met an x or dy value
-                                 of magnitude >= 65536 (or inf / NaN), which its fp16
-                                 weight-gradient operands cannot hold */
+  MOE_ERR_FP16_RANGE = -6     /* (device error word) moe_expert_mlp_bwd met inf / NaN or a
+                                 magnitude of 2^60 or more in x or dy, or one of its scaled
+                                 fp16 intermediates overflowed (see moe_expert_mlp_bwd) */
 } moe_status_t;
 
 /* Version of this ABI (MOE_ABI_VERSION). */
@@ -159,10 +159,19 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *      also runs the fp16 residuals of the rounded intermediates (compensated operands),
  *      and one with more padded rows than the shape's dW chunk (moe_tuning_t, default
  *      4096) is split over several tiles whose parts are TMA reduce-added.  Experts with
- *      no rows get exactly zero.  x, dy and the intermediates must stay within the fp16
- *      range (|v| < 65504): an x or dy value outside it is reported in the device error
- *      word as MOE_ERR_FP16_RANGE (the results of that call are then not meaningful); the
- *      intermediates are not checked.
+ *      no rows get exactly zero.
+ *   Range of the fp16 operands: every fp16 tensor is scaled by a power of two chosen on
+ *   the GPU from max|x| and max|dy| (ex, ey = their floor(log2), reduced first in the
+ *   workspace): x by 2^(14-ex), dy by 2^(14-ey), w*dA by 2^(8-ey), dG and dU by
+ *   2^(8-ey-ex), w*act by 2^(8-2ex); the weight-gradient epilogues multiply by the
+ *   inverse powers in fp32.  Scaling by 2^k is exact, so the results do not depend on the
+ *   scale of dy (scaling dy by 2^k scales every gradient by exactly 2^k) and fp16's narrow
+ *   exponent range costs nothing for max|x|, max|dy| in [2^-59, 2^60).  Reported in the
+ *   device error word as MOE_ERR_FP16_RANGE (the results of that call are then not
+ *   meaningful): inf / NaN or a magnitude of 2^60 or more in x or dy, and a scaled
+ *   intermediate that overflows fp16 (the scales leave about 2^6 of headroom over the
+ *   magnitudes of dy, x * dy and x^2 respectively, i.e. weights with row norms up to
+ *   about 64).
  *   dy [T,D] bf16, x_perm/perm_src/w_perm/offsets/counts (counts may be NULL) from
  *   moe_route_permute, weights as in the forward -- all device.  x [T,D] bf16 (device) or
  *   NULL: the unsorted input of the forward; when given, step 4's fp16 copy of the sorted
@@ -235,15 +244,18 @@ int moe_router_backward(const int32_t* topk_ids, const float* topk_w, const floa
  * Arguments, outputs and results are exactly those of moe_route_permute (bit for bit)
  * minus `workspace`.  The per-chunk expert counters live instead in one fixed 1 MiB
  * array inside the library (every GPU that loads the library keeps it until the
- * process exits), so E * ceil(T*K / 256) must not exceed 262080; larger sizes return
+ * process exits), so E * ceil(T*K / 256) must not exceed 262144; larger sizes return
  * MOE_ERR_UNSUPPORTED before anything is launched.  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library call.
  *
- * The first call on each device looks up the array's device address (with that device
- * current); make that first call before any stream capture.  All calls share the one
- * array, so two calls whose kernels overlap on the GPU (different streams, or different
- * host threads) race and corrupt each other's result; serialise them.  Expert ids
- * outside [0, E) are skipped without being reported (moe_route_permute reports them).
+ * Every call looks up the array's device address on the current device (with
+ * cudaGetSymbolAddress), so the address stays right across a cudaDeviceReset.  The
+ * first call on each device also loads the library's device code; make that first call
+ * before any stream capture.  All calls share the one array, whose counters every call
+ * rewrites before reading them, so two calls whose kernels overlap on the GPU (different
+ * streams, or different host threads) race and corrupt each other's result; serialise
+ * them.  Expert ids outside [0, E) are skipped without being reported
+ * (moe_route_permute reports them in its workspace's error word).
  */
 int moe_route_permute_noalloc(const int32_t* topk_ids, const float* topk_w,
                               const moe_bf16_t* x, int T, int K, int E, int D, int align,

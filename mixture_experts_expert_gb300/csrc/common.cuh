@@ -362,4 +362,43 @@ __device__ __forceinline__ float sigmoidf_fast(float z) {
   return __fdividef(1.0f, 1.0f + __expf(-z));
 }
 
+// ---------------------------------------------------------------- power-of-two scales
+// Exponents are clamped to [-59, 59], so that every scale and every inverse scale below is
+// one or two normal fp32 powers of two.
+constexpr int kScaleExpClamp = 59;
+
+// floor(log2 v) of a non-negative fp32 bit pattern, clamped to [-59, 59]; 0 for zero and
+// for inf / NaN.
+__device__ __forceinline__ int floor_log2_bits(uint32_t b) {
+  if (b == 0u || b >= 0x7f800000u) return 0;
+  // a subnormal b is its own mantissa: v = b * 2^-149, floor(log2 v) = 31 - clz(b) - 149
+  const int e = (b >> 23) ? static_cast<int>(b >> 23) - 127 : -118 - __clz(static_cast<int>(b));
+  return e < -kScaleExpClamp ? -kScaleExpClamp : (e > kScaleExpClamp ? kScaleExpClamp : e);
+}
+
+// 2^k as an fp32 value (k clamped to the normal range [-126, 127]).
+__device__ __forceinline__ float pow2f(int k) {
+  k = k < -126 ? -126 : (k > 127 ? 127 : k);
+  return __int_as_float((k + 127) << 23);
+}
+
+// Exponents of the backward's scales (see kX16Exp ... kActExp): floor(log2) of max|x| and
+// max|dY|.
+struct BwdExps {
+  int ex, ey;
+};
+
+__device__ __forceinline__ BwdExps load_bwd_exps(const uint32_t* maxabs) {
+  BwdExps s;
+  s.ex = floor_log2_bits(__ldg(maxabs));
+  s.ey = floor_log2_bits(__ldg(maxabs + 1));
+  return s;
+}
+
+// Bit 15 of a 16-bit half set where the packed fp16 value is inf or NaN (exponent all ones):
+// the scaled value overflowed fp16.  OR the results over a tile, then test 0x80008000.
+__device__ __forceinline__ uint32_t f16x2_overflow_bits(uint32_t packed) {
+  return (packed & 0x7c007c00u) + 0x04000400u;
+}
+
 }  // namespace moe

@@ -621,6 +621,19 @@ __device__ __forceinline__ void to_f16_residual(float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] -= __half2float(__float2half_rn(v[i]));
 }
 
+// Whether any of the values rounds to an fp16 infinity (|v| >= 65520).
+__device__ __forceinline__ bool f16_overflows(const float (&v)[32]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m >= 65520.f;
+}
+
+// Scaled fp16 intermediates that overflowed: one report per warp.
+__device__ __forceinline__ void report_f16_overflow(const GemmParams& p, bool ovf) {
+  if (__any_sync(0xffffffffu, ovf) && (threadIdx.x & 31) == 0) report_error(p.err, kDevFp16Range);
+}
+
 // A zeroed box in the next ring buffer.
 template <int NBUF, int BYTES>
 __device__ __forceinline__ uint8_t* stage_zero(uint8_t* stg, int& ring, int lane) {
@@ -670,14 +683,18 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
   } else if constexpr (KIND == GemmKind::DA) {
     const int x = ti.n0 + 128 * rank + 32 * q;
     const bool want_lo = dw_compensated(p, ti.e);
+    const float fa = pow2f(kDAExp - load_bwd_exps(p.maxabs).ey);
+    bool ovf = false;
     for (int j = 0; j < nch; ++j) {
-      const float wl = __ldg(p.w_perm + ti.m0 + 32 * j + lane);   // router weight of row lane
+      // router weight of row `lane`, times dA's power-of-two scale (exact)
+      const float wl = __ldg(p.w_perm + ti.m0 + 32 * j + lane) * fa;
       uint32_t r[32];
       tmem_ld32(tb + 32 * j, r);
       tmem_ld_wait(r);
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __shfl_sync(0xffffffffu, wl, i) * __uint_as_float(r[i]);
+      ovf |= f16_overflows(v);
       uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
       stage_16_col(buf, lane, v, true);
       store_box(&p.mapO0, buf, x, ti.m0 + 32 * j, lane, false);
@@ -693,6 +710,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
       store_zero_rows(&p.mapO0, z, x, ti, lane);
       if (want_lo) store_zero_rows(&p.mapO1, z, x, ti, lane);
     }
+    report_f16_overflow(p, ovf);
     return true;
   } else {
     const int pi = q & 1;
@@ -726,8 +744,15 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
     // gate warp: act columns f0 .. f0+31
     const int f0 = ti.n0 + 64 * rank + 32 * pi;
     bool want_lo = false;
-    if constexpr (KIND == GemmKind::BwdGU)
+    bool ovf = false;
+    float fw = 1.f, fh = 1.f, fb = 1.f;   // backward: scales of w*act, dH fp16, dH bf16
+    if constexpr (KIND == GemmKind::BwdGU) {
       want_lo = dw_compensated(p, ti.e);
+      const BwdExps sc = load_bwd_exps(p.maxabs);
+      fw = pow2f(kActExp - 2 * sc.ex);
+      fh = pow2f(kDHExp - kDAExp - sc.ex);   // dA arrives scaled by 2^(kDAExp - ey)
+      fb = pow2f(sc.ey - kDAExp);
+    }
     for (int j = 0; j < nch; ++j) {
       const int row0 = ti.m0 + 32 * j;
       uint32_t g[32];
@@ -754,7 +779,7 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
         stage_16_col(buf, lane, v, false);
         store_box(&p.mapO0, buf, f0, row0, lane, false);
       } else {
-        const float wl = __ldg(p.w_perm + row0 + lane);
+        const float wl = __ldg(p.w_perm + row0 + lane) * fw;
         const unsigned short* da = reinterpret_cast<const unsigned short*>(p.dA) +
                                    static_cast<size_t>(row0) * p.I + f0 + lane;
         float d[32];
@@ -768,12 +793,13 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
           for (int i = 0; i < 32; ++i)
             d[i] += __half2float(__ushort_as_half(__ldg(dl + static_cast<size_t>(i) * p.I)));
         }
-        // w * act (fp16; dW_down operand)
+        // w * act (scaled fp16; dW_down operand)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float gv = __uint_as_float(g[i]);
           v[i] = __shfl_sync(0xffffffffu, wl, i) * gv * sigmoidf_fast(gv) * u[i];
         }
+        ovf |= f16_overflows(v);
         uint8_t* b0 = ring_next<R16, 2048>(stg, ring, lane);
         stage_16_col(b0, lane, v, true);
         store_box(&p.mapO0, b0, f0, row0, lane, false);
@@ -783,16 +809,22 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
           stage_16_col(c0, lane, v, true);
           store_box(&p.mapO3, c0, f0, row0, lane, false);
         }
-        // dG = dA U silu'(G)
+        // dG = dA U silu'(G): bf16 unscaled (dX operand), fp16 scaled (dW operand)
+        float vs[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float gv = __uint_as_float(g[i]);
           const float sg = sigmoidf_fast(gv);
-          v[i] = d[i] * u[i] * sg * (1.0f + gv * (1.0f - sg));
+          const float dg = d[i] * u[i] * sg * (1.0f + gv * (1.0f - sg));
+          v[i] = dg * fb;
+          vs[i] = dg * fh;
         }
         uint8_t* b1 = ring_next<R16, 2048>(stg, ring, lane);
         stage_16_col(b1, lane, v, false);
         store_box(&p.mapO1, b1, f0, row0, lane, false);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = vs[i];
+        ovf |= f16_overflows(v);
         uint8_t* b2 = ring_next<R16, 2048>(stg, ring, lane);
         stage_16_col(b2, lane, v, true);
         store_box(&p.mapO2, b2, f0, row0, lane, false);
@@ -806,11 +838,16 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float gv = __uint_as_float(g[i]);
-          v[i] = d[i] * gv * sigmoidf_fast(gv);
+          const float du = d[i] * gv * sigmoidf_fast(gv);
+          v[i] = du * fb;
+          vs[i] = du * fh;
         }
         uint8_t* b3 = ring_next<R16, 2048>(stg, ring, lane);
         stage_16_col(b3, lane, v, false);
         store_box(&p.mapO1, b3, p.I + f0, row0, lane, false);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = vs[i];
+        ovf |= f16_overflows(v);
         uint8_t* b4 = ring_next<R16, 2048>(stg, ring, lane);
         stage_16_col(b4, lane, v, true);
         store_box(&p.mapO2, b4, p.I + f0, row0, lane, false);
@@ -837,7 +874,106 @@ __device__ __forceinline__ bool epilogue_swap(const GemmParams& p, GemmBarriers*
         }
       }
     }
+    if constexpr (KIND == GemmKind::BwdGU) report_f16_overflow(p, ovf);
     return true;
+  }
+}
+
+// Backward gate/up epilogue, one 32-column chunk c of a regular tile: recomputed G, U from
+// TMEM and dA from memory give w*act (scaled fp16), dG and dU (bf16 and scaled fp16) and,
+// for experts with compensated dW operands (LO), the fp16 residuals of the three fp16
+// outputs.  `ovf` collects fp16 overflow bits (see f16x2_overflow_bits).
+template <int R16, bool LO>
+__device__ __forceinline__ void bwd_gu_chunk(const GemmParams& p, uint32_t tb, int c,
+                                             const uint4* da_row, const uint4* dl_row, float wr,
+                                             float fh, float fb, uint8_t* stg, int& ring, int row,
+                                             int lane, uint32_t& ovf, int n0) {
+  uint4 d4[4], l4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = __ldg(da_row + 4 * c + i);   // w-scaled dA, fp16
+  if constexpr (LO) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l4[i] = __ldg(dl_row + 4 * c + i);   // its residual
+  }
+  uint32_t g[32], u[32];
+  tmem_ld32(tb + 32 * c, g);
+  tmem_ld32(tb + 128 + 32 * c, u);
+  tmem_ld_wait(g);
+  tmem_ld_after_wait(u);
+  const __half2* h2 = reinterpret_cast<const __half2*>(d4);
+  const __half2* l2 = reinterpret_cast<const __half2*>(l4);
+  uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16], la[16], lg[16], lu[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float2 da = __half22float2(h2[i]);   // dA of this pair of columns (plus its residual)
+    if constexpr (LO) {
+      const float2 dl = __half22float2(l2[i]);
+      da.x += dl.x;
+      da.y += dl.y;
+    }
+    float r[2][3];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float gv = __uint_as_float(g[2 * i + h]);
+      const float uv = __uint_as_float(u[2 * i + h]);
+      const float dv = h ? da.y : da.x;
+      const float sg = sigmoidf_fast(gv);
+      const float si = gv * sg;
+      r[h][0] = wr * si * uv;                              // w * act (dW_down operand)
+      r[h][1] = dv * uv * sg * (1.0f + gv * (1.0f - sg));  // dG (scaled as dA)
+      r[h][2] = dv * si;                                   // dU (scaled as dA)
+    }
+    pa[i] = pack_f16x2(r[0][0], r[1][0]);
+    pg[i] = pack_bf16x2(r[0][1] * fb, r[1][1] * fb);
+    pu[i] = pack_bf16x2(r[0][2] * fb, r[1][2] * fb);
+    const float g0 = r[0][1] * fh, g1 = r[1][1] * fh;
+    const float u0 = r[0][2] * fh, u1 = r[1][2] * fh;
+    pg16[i] = pack_f16x2(g0, g1);
+    pu16[i] = pack_f16x2(u0, u1);
+    ovf |= f16x2_overflow_bits(pa[i]) | f16x2_overflow_bits(pg16[i]) |
+           f16x2_overflow_bits(pu16[i]);
+    if constexpr (LO) {
+      la[i] = f16x2_residual(pa[i], r[0][0], r[1][0]);
+      lg[i] = f16x2_residual(pg16[i], g0, g1);
+      lu[i] = f16x2_residual(pu16[i], u0, u1);
+    }
+  }
+  const int col = n0 + 32 * c;
+  // boxes are staged in groups of up to R16 (the ring) and fenced once per group
+  ring_reserve<R16, 3>(lane);
+  uint8_t* b0 = ring_slot<R16, 2048>(stg, ring);
+  stage_16_row(b0, lane, pa);
+  uint8_t* b1 = ring_slot<R16, 2048>(stg, ring);
+  stage_16_row(b1, lane, pg);
+  uint8_t* b2 = ring_slot<R16, 2048>(stg, ring);
+  stage_16_row(b2, lane, pu);
+  fence_boxes();
+  issue_box(&p.mapO0, b0, col, row, lane);        // w*act, fp16
+  issue_box(&p.mapO1, b1, col, row, lane);        // dG, bf16
+  issue_box(&p.mapO1, b2, p.I + col, row, lane);  // dU, bf16
+  __syncwarp();
+  ring_reserve<R16, 2>(lane);
+  uint8_t* b3 = ring_slot<R16, 2048>(stg, ring);
+  stage_16_row(b3, lane, pg16);
+  uint8_t* b4 = ring_slot<R16, 2048>(stg, ring);
+  stage_16_row(b4, lane, pu16);
+  fence_boxes();
+  issue_box(&p.mapO2, b3, col, row, lane);        // dG, fp16
+  issue_box(&p.mapO2, b4, p.I + col, row, lane);  // dU, fp16
+  __syncwarp();
+  if constexpr (LO) {
+    ring_reserve<R16, 3>(lane);
+    uint8_t* c0 = ring_slot<R16, 2048>(stg, ring);
+    stage_16_row(c0, lane, la);
+    uint8_t* c1 = ring_slot<R16, 2048>(stg, ring);
+    stage_16_row(c1, lane, lg);
+    uint8_t* c2 = ring_slot<R16, 2048>(stg, ring);
+    stage_16_row(c2, lane, lu);
+    fence_boxes();
+    issue_box(&p.mapO3, c0, col, row, lane);        // w*act residual
+    issue_box(&p.mapO4, c1, col, row, lane);        // dG residual
+    issue_box(&p.mapO4, c2, p.I + col, row, lane);  // dU residual
+    __syncwarp();
   }
 }
 
@@ -936,10 +1072,12 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
           store_box(&p.mapO0, buf, ti.n0 + 32 * c, row, lane, false);
         }
       } else if constexpr (KIND == GemmKind::DA) {
-        const float wr = __ldg(p.w_perm + row + lane);   // router weight of this thread's row
+        // router weight of this thread's row times dA's power-of-two scale (exact)
+        const float wr = __ldg(p.w_perm + row + lane) * pow2f(kDAExp - load_bwd_exps(p.maxabs).ey);
         const bool want_lo =
             dw_compensated(p, ti.e);
         const int nch = p.tile_n / 32;
+        uint32_t ovf = 0;
         for (int c = 0; c < nch; ++c) {
           uint32_t r[32];
           tmem_ld32(tb + 32 * c, r);
@@ -950,7 +1088,8 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
             const float v0 = wr * __uint_as_float(r[2 * i]);
             const float v1 = wr * __uint_as_float(r[2 * i + 1]);
             pk[i] = pack_f16x2(v0, v1);
-            lo[i] = f16x2_residual(pk[i], v0, v1);
+            ovf |= f16x2_overflow_bits(pk[i]);
+            if (want_lo) lo[i] = f16x2_residual(pk[i], v0, v1);
           }
           uint8_t* buf = ring_next<R16, 2048>(stg, ring, lane);
           stage_16_row(buf, lane, pk);
@@ -961,9 +1100,17 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
             store_box(&p.mapO1, lb, ti.n0 + 32 * c, row, lane, false);
           }
         }
+        report_f16_overflow(p, (ovf & 0x80008000u) != 0u);
       } else if constexpr (KIND == GemmKind::BwdGU) {
         const int my_row = row + lane;
-        const float wr = __ldg(p.w_perm + my_row);
+        const BwdExps sc = load_bwd_exps(p.maxabs);
+        // w * act scaled by 2^(kActExp - 2 ex); dA arrives scaled by 2^(kDAExp - ey), so dG
+        // and dU take 2^(kDHExp - kDAExp - ex) for their fp16 copies and 2^(ey - kDAExp) back
+        // to their true values for the bf16 ones
+        const float wr = __ldg(p.w_perm + my_row) * pow2f(kActExp - 2 * sc.ex);
+        const float fh = pow2f(kDHExp - kDAExp - sc.ex);
+        const float fb = pow2f(sc.ey - kDAExp);
+        uint32_t ovf = 0;
         // rows of an expert with compensated dW operands also get the fp16 residuals
         const bool want_lo =
             dw_compensated(p, ti.e);
@@ -972,107 +1119,33 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmBarriers* bars
         const uint4* dl_row =
             reinterpret_cast<const uint4*>(p.dA_lo + static_cast<size_t>(my_row) * p.I + ti.n0);
         for (int c = 0; c < 4; ++c) {
-          uint4 d4[4], l4[4];
-  #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = __ldg(da_row + 4 * c + i);   // w-scaled dA, fp16
-          if (want_lo) {
-  #pragma unroll
-            for (int i = 0; i < 4; ++i) l4[i] = __ldg(dl_row + 4 * c + i);   // its residual
-          }
-          uint32_t g[32], u[32];
-          tmem_ld32(tb + 32 * c, g);
-          tmem_ld32(tb + 128 + 32 * c, u);
-          tmem_ld_wait(g);
-          tmem_ld_after_wait(u);
-          float da[32];
-          {
-            const __half2* h2 = reinterpret_cast<const __half2*>(d4);
-  #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 f = __half22float2(h2[i]);
-              da[2 * i] = f.x;
-              da[2 * i + 1] = f.y;
-            }
-            if (want_lo) {
-              const __half2* l2 = reinterpret_cast<const __half2*>(l4);
-  #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float2 f = __half22float2(l2[i]);
-                da[2 * i] += f.x;
-                da[2 * i + 1] += f.y;
-              }
-            }
-          }
-          uint32_t pa[16], pg[16], pu[16], pg16[16], pu16[16], la[16], lg[16], lu[16];
-  #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float r[2][3];
-  #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float gv = __uint_as_float(g[2 * i + h]);
-              const float uv = __uint_as_float(u[2 * i + h]);
-              const float dv = da[2 * i + h];
-              const float sg = sigmoidf_fast(gv);
-              const float si = gv * sg;
-              r[h][0] = wr * si * uv;                              // w * act (dW_down operand)
-              r[h][1] = dv * uv * sg * (1.0f + gv * (1.0f - sg));  // dG
-              r[h][2] = dv * si;                                   // dU
-            }
-            pa[i] = pack_f16x2(r[0][0], r[1][0]);
-            pg[i] = pack_bf16x2(r[0][1], r[1][1]);
-            pu[i] = pack_bf16x2(r[0][2], r[1][2]);
-            pg16[i] = pack_f16x2(r[0][1], r[1][1]);
-            pu16[i] = pack_f16x2(r[0][2], r[1][2]);
-            la[i] = f16x2_residual(pa[i], r[0][0], r[1][0]);
-            lg[i] = f16x2_residual(pg16[i], r[0][1], r[1][1]);
-            lu[i] = f16x2_residual(pu16[i], r[0][2], r[1][2]);
-          }
-          const int col = ti.n0 + 32 * c;
-          // boxes are staged in groups of up to R16 (the ring) and fenced once per group
-          ring_reserve<R16, 3>(lane);
-          uint8_t* b0 = ring_slot<R16, 2048>(stg, ring);
-          stage_16_row(b0, lane, pa);
-          uint8_t* b1 = ring_slot<R16, 2048>(stg, ring);
-          stage_16_row(b1, lane, pg);
-          uint8_t* b2 = ring_slot<R16, 2048>(stg, ring);
-          stage_16_row(b2, lane, pu);
-          fence_boxes();
-          issue_box(&p.mapO0, b0, col, row, lane);        // w*act, fp16
-          issue_box(&p.mapO1, b1, col, row, lane);        // dG, bf16
-          issue_box(&p.mapO1, b2, p.I + col, row, lane);  // dU, bf16
-          __syncwarp();
-          ring_reserve<R16, 2>(lane);
-          uint8_t* b3 = ring_slot<R16, 2048>(stg, ring);
-          stage_16_row(b3, lane, pg16);
-          uint8_t* b4 = ring_slot<R16, 2048>(stg, ring);
-          stage_16_row(b4, lane, pu16);
-          fence_boxes();
-          issue_box(&p.mapO2, b3, col, row, lane);        // dG, fp16
-          issue_box(&p.mapO2, b4, p.I + col, row, lane);  // dU, fp16
-          __syncwarp();
-          if (want_lo) {
-            ring_reserve<R16, 3>(lane);
-            uint8_t* c0 = ring_slot<R16, 2048>(stg, ring);
-            stage_16_row(c0, lane, la);
-            uint8_t* c1 = ring_slot<R16, 2048>(stg, ring);
-            stage_16_row(c1, lane, lg);
-            uint8_t* c2 = ring_slot<R16, 2048>(stg, ring);
-            stage_16_row(c2, lane, lu);
-            fence_boxes();
-            issue_box(&p.mapO3, c0, col, row, lane);        // w*act residual
-            issue_box(&p.mapO4, c1, col, row, lane);        // dG residual
-            issue_box(&p.mapO4, c2, p.I + col, row, lane);  // dU residual
-            __syncwarp();
-          }
+          if (want_lo) bwd_gu_chunk<R16, true>(p, tb, c, da_row, dl_row, wr, fh, fb, stg, ring, row,
+                                             lane, ovf, ti.n0);
+          else bwd_gu_chunk<R16, false>(p, tb, c, da_row, dl_row, wr, fh, fb, stg, ring, row, lane,
+                                        ovf, ti.n0);
         }
+        report_f16_overflow(p, (ovf & 0x80008000u) != 0u);
       } else {  // DwGU, DwD: fp32 out, plain store or split-K reduce-add
+        // undo the operands' power-of-two scales (exact): dW_gate|up = x16^T dH16 carries
+        // 2^(kX16Exp - ex) 2^(kDHExp - ey - ex); dW_down = wact16^T dy16 carries
+        // 2^(kActExp - 2 ex) 2^(kDy16Exp - ey).  Two factors, each a normal fp32 power of
+        // two for |ex|, |ey| <= 59 (their product alone could leave fp32's range).
+        const BwdExps sc = load_bwd_exps(p.maxabs);
+        float f1, f2;
+        if constexpr (KIND == GemmKind::DwGU) {
+          f1 = pow2f(sc.ex - kX16Exp);
+          f2 = pow2f(sc.ex + sc.ey - kDHExp);
+        } else {
+          f1 = pow2f(2 * sc.ex - kActExp);
+          f2 = pow2f(sc.ey - kDy16Exp);
+        }
         for (int c = 0; c < 8; ++c) {
           uint32_t r[32];
           tmem_ld32(tb + 32 * c, r);
           tmem_ld_wait(r);
           float v[32];
   #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * f1 * f2;
           uint8_t* buf = ring_next<R32, 4096>(stg, ring, lane);
           stage_f32_row(buf, lane, v);
           const int col = ti.n0 + 32 * c;

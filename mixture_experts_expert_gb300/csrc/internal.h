@@ -16,8 +16,28 @@ enum DevErr : int {
   kDevTimeoutMma = 3,       // MMA issuer gave up waiting on data or TMEM
   kDevTimeoutEpilogue = 4,  // epilogue gave up waiting on an accumulator
   kDevTimeoutRoute = 6,     // the fused routing kernel gave up at a grid barrier
-  kDevFp16Range = 7,        // an x or dY value outside the fp16 range (the dW operands)
+  kDevFp16Range = 7,        // x or dY holds inf / NaN or a magnitude of 2^60 or more, or a
+                            // scaled fp16 intermediate of the backward overflowed
 };
+
+// Power-of-two scales of the backward's fp16 operands.  The backward first reduces
+// max|x| and max|dY| (their fp32 bit patterns, in the workspace header at kMaxAbsOffset);
+// with ex = floor(log2 max|x|), ey = floor(log2 max|dY|) (each clamped to [-59, 59]) the
+// fp16 tensors hold
+//   x16    = x      * 2^(kX16Exp - ex)            dy16 = dY * 2^(kDy16Exp - ey)
+//   dA16   = w dA   * 2^(kDAExp - ey)             dH16 = [dG dU] * 2^(kDHExp - ey - ex)
+//   wact16 = w act  * 2^(kActExp - 2 ex)
+// and the weight-gradient epilogues multiply by the inverse powers.  Multiplying by 2^k
+// changes only the exponent, so the scaling itself is exact; it keeps the largest x and
+// dY values just below 2^15 and the intermediates (linear in dY; dG, dU also in x; act
+// quadratic in x) near 2^8 - 2^10, far from both ends of fp16's range, for max|x| and
+// max|dY| anywhere in [2^-59, 2^60).
+constexpr int kX16Exp = 14;
+constexpr int kDy16Exp = 14;
+constexpr int kDAExp = 8;
+constexpr int kDHExp = 8;
+constexpr int kActExp = 8;
+constexpr size_t kMaxAbsOffset = 256;   // two uint32 in the workspace header
 
 // Identifiers of every kernel the library launches (for launch counting and timing).
 enum KernelId : int {
@@ -44,6 +64,12 @@ enum KernelId : int {
 };
 
 const char* kernel_name(int id);
+
+// Argument checks shared by the entry points (moe_api.cu).
+bool basic_sizes_ok(int T, int K, int E, int align);   // T, K, E, align and the sizes they imply
+size_t capacity_of(int T, int K, int E, int align);    // moe_capacity without the checks
+bool aligned16(const void* p);
+int check_device();   // MOE_OK, MOE_ERR_UNSUPPORTED (not sm_103) or MOE_ERR_CUDA
 
 // Brackets one launch with timing events when timing is on; counts launches.
 struct LaunchScope {
@@ -89,6 +115,7 @@ struct GemmParams {
   const float* w_perm;     // [cap] router weight per sorted row (DA, BwdGU)
   const uint16_t* dA;      // [cap, I] router-weighted dA, fp16 (BwdGU reads it)
   const uint16_t* dA_lo;   // [cap, I] its fp16 residual (rows of compensated experts)
+  const uint32_t* maxabs;  // backward kinds: {max|x|, max|dY|} as fp32 bits (scales)
   int* err;                // device error word
   int E, D, I;
   int n_tiles;             // N tiles per M tile
@@ -116,13 +143,16 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, con
                                uint16_t* dst, int kernel_id, cudaStream_t s);
 
 // Backward operand preparation for every sorted row s < offsets[E]:
-//   dy_perm[s] = dy[perm_src[s] / K] (bf16, unscaled), dy16[s] = fp16 of the same row,
-//   x16[s] = fp16(x[perm_src[s] / K]) (from x_perm[s] when x is null); zero rows on padding.
-// `inv` ([T*K] int32 scratch) receives each routed slot's sorted row (-1: none).
+//   dy_perm[s] = dy[perm_src[s] / K] (bf16, unscaled), dy16[s] = fp16 of the same row
+//   scaled by 2^(kDy16Exp - ey), x16[s] = fp16(x[perm_src[s] / K] * 2^(kX16Exp - ex))
+//   (from x_perm[s] when x is null); zero rows on padding.
+// A first kernel reduces max|x| (x, or x_perm's routed rows) and max|dY| into `maxabs`
+// (zeroed here first) and records each routed slot's sorted row in `inv` ([T*K] scratch).
 cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
                                  const int32_t* perm_src, const int32_t* offsets, int T, int E,
                                  int K, int D, int cap, int32_t* inv, uint16_t* dy_perm,
-                                 uint16_t* dy16, uint16_t* x16, int* err, cudaStream_t s);
+                                 uint16_t* dy16, uint16_t* x16, uint32_t* maxabs, int* err,
+                                 cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
                            int T, int K, int D, uint16_t* out, cudaStream_t s);

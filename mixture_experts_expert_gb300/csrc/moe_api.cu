@@ -160,14 +160,14 @@ static bool map_store_f32(CUtensorMap* m, const void* b, uint64_t inner, uint64_
 }
 
 // ------------------------------------------------------------------ sizes
-static bool basic_sizes_ok(int T, int K, int E, int align) {
+bool basic_sizes_ok(int T, int K, int E, int align) {
   if (T < 0 || K < 1 || K > 32 || E < 1 || E > kMaxExperts || align < 1) return false;
   const long long R = static_cast<long long>(T) * K;
   const long long cap = R + static_cast<long long>(E) * (align - 1) + align;
   return R < (1ll << 31) && cap < (1ll << 31);
 }
 
-static size_t capacity_of(int T, int K, int E, int align) {
+size_t capacity_of(int T, int K, int E, int align) {
   const size_t R = static_cast<size_t>(T) * K;
   const size_t c = R + static_cast<size_t>(E) * (align - 1);
   return (c + align - 1) / align * align;
@@ -220,9 +220,9 @@ static WsLayout ws_layout(int T, int K, int E, int D, int I, int align) {
   return L;
 }
 
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-static int check_device() {
+int check_device() {
   const DevFacts* f = dev_facts();
   if (!f) return MOE_ERR_CUDA;
   if (f->major != 10 || f->minor != 3) return MOE_ERR_UNSUPPORTED;
@@ -324,13 +324,14 @@ MOE_EXPORT const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case MOE_ERR_BAD_INDEX: return "expert id out of range";
-    case MOE_ERR_FP16_RANGE: return "x or dY value outside the fp16 range";
+    case MOE_ERR_FP16_RANGE: return "value outside the range of the backward's scaled fp16 operands";
     default: return "unknown status";
   }
 }
 
-// Workspace header: [0] device error word; at kRouteSyncOffset the fused routing kernel's
-// grid-barrier counters {arrivals, exits} (zero between launches).
+// Workspace header: [0] device error word; at kMaxAbsOffset the backward's {max|x|, max|dY|}
+// (fp32 bits); at kRouteSyncOffset the fused routing kernel's grid-barrier counters
+// {arrivals, exits} (zero between launches).
 constexpr size_t kRouteSyncOffset = 512;
 
 MOE_EXPORT size_t moe_capacity(int T, int K, int E, int align) {
@@ -497,11 +498,14 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   moe_bf16_t* xp16 = reinterpret_cast<moe_bf16_t*>(ws + L.xp16);
   void* act_lo = ws + L.act_lo;
   void* dh16_lo = ws + L.dh16_lo;
+  uint32_t* maxabs = reinterpret_cast<uint32_t*>(ws + kMaxAbsOffset);
 
-  // 1. routed expert-output gradient rows (unscaled; the router weight is applied to dA in
-  //    fp32) and the fp16 operand copies of the weight-gradient GEMMs
+  // 1. max|x| and max|dY| (the power-of-two scales of the fp16 operands), the routed
+  //    expert-output gradient rows (unscaled; the router weight is applied to dA in fp32)
+  //    and the scaled fp16 operand copies of the weight-gradient GEMMs
   e = launch_bwd_prep_rows(dy, x, x_perm, perm_src, offsets, T, E, K, D, static_cast<int>(cap),
-                           reinterpret_cast<int32_t*>(ws + L.inv), dyp, dyp16, xp16, err, s);
+                           reinterpret_cast<int32_t*>(ws + L.inv), dyp, dyp16, xp16, maxabs,
+                           err, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // 2. dA = w * dy_perm W_d^T (scaled in fp32, kept in fp16), then the gate/up recompute
@@ -510,6 +514,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   uint16_t* dA_lo = reinterpret_cast<uint16_t*>(ws + L.da_lo);
   GemmParams da{};
   da.offsets = offsets; da.counts = counts; da.w_perm = w_perm; da.err = err;
+  da.maxabs = maxabs;
   da.E = E; da.D = D; da.I = I;
   da.order = tun.order[MOE_GEMM_DA];
   da.swap_tails = tun.swap_tails;
@@ -528,7 +533,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams a{};
   a.offsets = offsets; a.counts = counts; a.w_perm = w_perm; a.dA = dA; a.dA_lo = dA_lo;
-  a.err = err;
+  a.err = err; a.maxabs = maxabs;
   a.E = E; a.D = D; a.I = I;
   a.order = tun.order[MOE_GEMM_BWD_GATE_UP];
   a.swap_tails = tun.swap_tails;
@@ -572,6 +577,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   const int max_chunks = E + static_cast<int>(cap / chunk) + 1;
   GemmParams g{};
   g.offsets = offsets; g.counts = counts; g.dw_prefix = dw_prefix; g.err = err;
+  g.maxabs = maxabs;
   g.E = E; g.D = D; g.I = I;
   g.dw_chunk_rows = chunk;
   ok = map_mnmajor(&g.mapA0, xp16, D, cap, 2, Elem::F16) &&
@@ -588,6 +594,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams d{};
   d.offsets = offsets; d.counts = counts; d.dw_prefix = dw_prefix; d.err = err;
+  d.maxabs = maxabs;
   d.E = E; d.D = D; d.I = I;
   d.dw_chunk_rows = chunk;
   ok = map_mnmajor(&d.mapA0, act, I, cap, 2, Elem::F16) &&

@@ -384,7 +384,7 @@ cudaError_t launch_route(const int32_t* ids, const float* w, const uint16_t* x, 
                                                          perm_src, inv_perm, w_perm);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if (x != nullptr) {
+  if (x != nullptr && R > 0) {
     e = launch_gather_rows(x, perm_src, nullptr, offsets, E, K, D, cap, x_perm, kKGatherX, s);
   }
   return e;
@@ -529,43 +529,103 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int32_t* perm_src, con
 }
 
 // ------------------------------------------------------------------ backward row prep
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 q) {
+// fp16 copy of eight bf16 values times 2^k (f = 2^k, exact: only the exponent moves).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 q, float f) {
   uint32_t* w = reinterpret_cast<uint32_t*>(&q);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
-    w[i] = pack_f16x2(f.x, f.y);
+    const float2 v = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
+    w[i] = pack_f16x2(v.x * f, v.y * f);
   }
   return q;
 }
 
-// Bit 15 of each 16-bit half set where the bf16 value's magnitude is at least 65536 (or
-// it is inf / NaN): values the fp16 copies of the weight-gradient operands cannot hold
-// (fp16 tops out at 65504; the largest bf16 below 65536 is 65280).
-__device__ __forceinline__ uint32_t fp16_overflow_bits(uint4 q) {
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(&q);
-  uint32_t r = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) r |= (w[i] & 0x7fff7fffu) + 0x38803880u;   // 0x4780 + 0x3880 = 0x8000
-  return r & 0x80008000u;
+// Largest magnitude among eight bf16 values, as bf16 bits in both halves of the result
+// (non-negative bf16 bit patterns order like their values).
+__device__ __forceinline__ uint32_t bf16x8_absmax_bits(uint4 q, uint32_t m) {
+  m = __vmaxu2(m, q.x & 0x7fff7fffu);
+  m = __vmaxu2(m, q.y & 0x7fff7fffu);
+  m = __vmaxu2(m, q.z & 0x7fff7fffu);
+  m = __vmaxu2(m, q.w & 0x7fff7fffu);
+  return m;
 }
 
-// Two kernels.  The first records each routed slot's sorted row (inv[j] = s).  A slot that
-// reached no row (an expert id outside [0, E)) keeps whatever its entry held, so the second
-// kernel accepts inv[j] = s only when perm_src[s] == j.  In the second, one warp per token reads the
-// token's dY and x rows once and writes them to its K sorted rows: dy_perm[s] = dy[t]
-// (bf16), dy16[s] = fp16(dy[t]), x16[s] = fp16(x[t]) (from the sorted copy of the row when
-// x is not given); its last E * kPadSlices blocks zero the three copies' padding rows.  In
-// sorted order the token rows would be re-read K times, mostly from DRAM once the copies
-// being written have pushed them out of L2.
+// max over both 16-bit halves, widened to the fp32 bit pattern of the same value
+__device__ __forceinline__ uint32_t bf16_pair_max_to_f32_bits(uint32_t m2) {
+  const uint32_t a = m2 & 0xffffu, b = m2 >> 16;
+  return (a > b ? a : b) << 16;
+}
+
+// Block-wide max of v (every thread of the block calls it), then one atomicMax.
+__device__ __forceinline__ void block_atomic_max(uint32_t v, uint32_t* dst, uint32_t* s_red) {
+  v = __reduce_max_sync(0xffffffffu, v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) s_red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < static_cast<int>(blockDim.x >> 5) ? s_red[lane] : 0u;
+    w = __reduce_max_sync(0xffffffffu, w);
+    if (lane == 0 && w != 0u) atomicMax(dst, w);
+  }
+  __syncthreads();
+}
+
+// Two kernels.  The first records each routed slot's sorted row (inv[j] = s; a slot that
+// reached no row, an expert id outside [0, E), keeps whatever its entry held, so the second
+// kernel accepts inv[j] = s only when perm_src[s] == j) and reduces max|x| (x, or the routed
+// rows of x_perm when x is not given) and max|dY| into maxabs[0], maxabs[1] (fp32 bits;
+// zeroed before the launch).  Inputs with inf / NaN or a magnitude of 2^60 or more are
+// reported: the scales cover finite magnitudes below 2^60.
+// In the second, one warp per token reads the token's dY and x rows once and writes them
+// to its K sorted rows: dy_perm[s] = dy[t] (bf16), dy16[s] = fp16(dy[t] * 2^(kDy16Exp - ey)),
+// x16[s] = fp16(x[t] * 2^(kX16Exp - ex)) (from the sorted copy of the row when x is not
+// given); its last E * kPadSlices blocks zero the three copies' padding rows.  In sorted
+// order the token rows would be re-read K times, mostly from DRAM once the copies being
+// written have pushed them out of L2.
 __global__ void __launch_bounds__(256) k_bwd_prep_pad(const int32_t* __restrict__ perm_src,
                                                       const int32_t* __restrict__ offsets, int E,
-                                                      int32_t* __restrict__ inv) {
+                                                      int32_t* __restrict__ inv,
+                                                      const uint16_t* __restrict__ x,
+                                                      const uint16_t* __restrict__ x_perm,
+                                                      const uint16_t* __restrict__ dy, int T,
+                                                      int D, uint32_t* maxabs, int* err) {
+  __shared__ uint32_t s_red[32];
   const int rows = __ldg(offsets + E);
-  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < rows; s += gridDim.x * blockDim.x) {
+  const int gtid = blockIdx.x * blockDim.x + threadIdx.x;
+  const int gthreads = gridDim.x * blockDim.x;
+  for (int s = gtid; s < rows; s += gthreads) {
     const int j = __ldg(perm_src + s);
     if (j >= 0) inv[j] = s;
   }
+  const size_t nvec_y = static_cast<size_t>(T) * D / 8;
+  const size_t nvec_x = x ? nvec_y : static_cast<size_t>(rows) * D / 8;
+  const uint4* px = reinterpret_cast<const uint4*>(x ? x : x_perm);
+  const uint4* py = reinterpret_cast<const uint4*>(dy);
+  uint32_t mx = 0, my = 0;
+  // four independent 16-byte loads in flight per thread and step
+  const size_t step = static_cast<size_t>(gthreads);
+  size_t v = gtid;
+  for (; v + 3 * step < nvec_x; v += 4 * step) {
+    const uint4 a = __ldg(px + v), b = __ldg(px + v + step), c = __ldg(px + v + 2 * step),
+                d = __ldg(px + v + 3 * step);
+    mx = bf16x8_absmax_bits(d, bf16x8_absmax_bits(c, bf16x8_absmax_bits(b,
+             bf16x8_absmax_bits(a, mx))));
+  }
+  for (; v < nvec_x; v += step) mx = bf16x8_absmax_bits(__ldg(px + v), mx);
+  v = gtid;
+  for (; v + 3 * step < nvec_y; v += 4 * step) {
+    const uint4 a = __ldg(py + v), b = __ldg(py + v + step), c = __ldg(py + v + 2 * step),
+                d = __ldg(py + v + 3 * step);
+    my = bf16x8_absmax_bits(d, bf16x8_absmax_bits(c, bf16x8_absmax_bits(b,
+             bf16x8_absmax_bits(a, my))));
+  }
+  for (; v < nvec_y; v += step) my = bf16x8_absmax_bits(__ldg(py + v), my);
+  mx = bf16_pair_max_to_f32_bits(mx);
+  my = bf16_pair_max_to_f32_bits(my);
+  // 2^60 = 0x5d800000: inf / NaN and magnitudes beyond the scales' range
+  if (mx >= 0x5d800000u || my >= 0x5d800000u) report_error(err, kDevFp16Range);
+  block_atomic_max(mx, maxabs, s_red);
+  block_atomic_max(my, maxabs + 1, s_red);
 }
 
 __global__ void __launch_bounds__(256) k_bwd_prep_rows(
@@ -573,7 +633,7 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     const uint16_t* __restrict__ x_perm, const int32_t* __restrict__ perm_src,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ inv, int T, int E, int K,
     int D, int token_blocks, uint16_t* __restrict__ dy_perm, uint16_t* __restrict__ dy16,
-    uint16_t* __restrict__ x16, int* err) {
+    uint16_t* __restrict__ x16, const uint32_t* __restrict__ maxabs) {
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int nvec = D >> 3;
@@ -601,6 +661,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
   }
   const int wpg = (token_blocks * blockDim.x) >> 5;
   const int rows = __ldg(offsets + E);
+  const BwdExps sc = load_bwd_exps(maxabs);
+  const float fx = pow2f(kX16Exp - sc.ex), fy = pow2f(kDy16Exp - sc.ey);
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += wpg) {
     const int my_s = slot_row(inv, perm_src, rows, t, K, lane);   // lane k: slot (t, k)
     const unsigned valid = __ballot_sync(0xffffffffu, my_s >= 0);
@@ -609,7 +671,6 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
     const uint4* sp = reinterpret_cast<const uint4*>(dy + static_cast<size_t>(t) * D);
     const uint4* xp = reinterpret_cast<const uint4*>(
         x ? x + static_cast<size_t>(t) * D : x_perm + static_cast<size_t>(s_first) * D);
-    uint32_t big = 0;   // bit 15 of a half set: a bf16 value the fp16 copies cannot hold
     // warp-uniform trip count: every lane takes part in the shuffles of every step
     for (int vb = 0; vb < nvec; vb += 32 * 4) {
       const int v0 = vb + lane;
@@ -619,10 +680,8 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
         const int v = v0 + 32 * u;
         if (v < nvec) {
           q[u] = __ldg(sp + v);
-          const uint4 xq = __ldg(xp + v);
-          big |= fp16_overflow_bits(q[u]) | fp16_overflow_bits(xq);
-          xh[u] = bf16x8_to_f16x8(xq);
-          h[u] = bf16x8_to_f16x8(q[u]);
+          xh[u] = bf16x8_to_f16x8_scaled(__ldg(xp + v), fx);
+          h[u] = bf16x8_to_f16x8_scaled(q[u], fy);
         }
       }
       for (int k = 0; k < K; ++k) {
@@ -643,27 +702,35 @@ __global__ void __launch_bounds__(256) k_bwd_prep_rows(
         }
       }
     }
-    if (__any_sync(0xffffffffu, big != 0) && lane == 0) report_error(err, kDevFp16Range);
   }
 }
 
 cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const uint16_t* x_perm,
                                  const int32_t* perm_src, const int32_t* offsets, int T, int E,
                                  int K, int D, int cap, int32_t* inv, uint16_t* dy_perm,
-                                 uint16_t* dy16, uint16_t* x16, int* err, cudaStream_t s) {
+                                 uint16_t* dy16, uint16_t* x16, uint32_t* maxabs, int* err,
+                                 cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(maxabs, 0, 2 * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
   if (T > 0) {
-    int blocks = (cap + 255) / 256;
-    if (blocks > 1024) blocks = 1024;
+    // enough blocks to stream x and dY (T * D values each) at full bandwidth: about four
+    // 16-byte vectors per thread and tensor, at most 2048 blocks
+    const long long vec = static_cast<long long>(T) * D / 8;
+    long long want = (vec + 1023) / 1024;
+    const long long rows_blocks = (static_cast<long long>(cap) + 255) / 256;
+    if (rows_blocks > want) want = rows_blocks;
+    const int blocks = static_cast<int>(want < 1 ? 1 : (want > 2048 ? 2048 : want));
     LaunchScope ls(kKBwdPrepPad, s);
-    k_bwd_prep_pad<<<blocks, 256, 0, s>>>(perm_src, offsets, E, inv);
-    cudaError_t e = cudaGetLastError();
+    k_bwd_prep_pad<<<blocks, 256, 0, s>>>(perm_src, offsets, E, inv, x, x_perm, dy, T, D, maxabs,
+                                          err);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const int token_blocks = (T + 7) / 8;
   LaunchScope ls(kKBwdPrepRows, s);
   k_bwd_prep_rows<<<token_blocks + E * kPadSlices, 256, 0, s>>>(
       dy, x, x_perm, perm_src, offsets, inv, T, E, K, D, token_blocks, dy_perm, dy16, x16,
-      err);
+      maxabs);
   return cudaGetLastError();
 }
 
@@ -822,37 +889,23 @@ cudaError_t launch_dw_prep(const int32_t* offsets, int E, int chunk_rows, int* d
 // allocation), or an engine whose device memory is carved out once up front and may not
 // grow afterwards.  moe_route_permute_noalloc serves them: its counters live in a
 // fixed array compiled into this library, so the caller passes only inputs and outputs.
-#include <mutex>
+#include "moe_gb300.h"
 
 namespace moe {
 namespace {
 
-// 1 MiB: the chunk counters need E * ceil(T*K / 256) ints, plus one error word.
+// 1 MiB: the chunk counters need E * ceil(T*K / 256) ints.
 constexpr int kNoAllocScratchInts = 1 << 18;
-constexpr int kNoAllocErrWord = kNoAllocScratchInts - 64;   // last 256 bytes: the error word
 static __device__ __align__(256) int32_t g_route_scratch[kNoAllocScratchInts];
 
-std::mutex g_noalloc_mu;
-int32_t* g_noalloc_scratch[64] = {};   // device address of g_route_scratch, per device
-
-// Host code cannot use g_route_scratch's name as a device pointer; look the address up once
-// per device (with that device current) and keep it.
+// Host code cannot use g_route_scratch's name as a device pointer: its device address is
+// looked up on the current device at every call (cheap once the library's device code is
+// loaded), so that a context torn down and made again (cudaDeviceReset) never leaves a
+// stale address behind.
 int32_t* noalloc_scratch_for_current_device(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= 64) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (g_noalloc_scratch[dev] == nullptr) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_noalloc_scratch[dev] = static_cast<int32_t*>(p);
-  }
-  return g_noalloc_scratch[dev];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_route_scratch);
+  return *err == cudaSuccess ? static_cast<int32_t*>(p) : nullptr;
 }
 
 }  // namespace
@@ -863,36 +916,25 @@ extern "C" __attribute__((visibility("default"))) int moe_route_permute_noalloc(
     int align, int32_t* counts, int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
     float* w_perm, uint16_t* x_perm, void* stream) {
   using namespace moe;
-  // the same argument rules as moe_route_permute
-  if (T < 0 || K < 1 || K > 32 || E < 1 || E > 1024 || align < 1) return -1;
-  const long long R = static_cast<long long>(T) * K;
-  const long long capl = R + static_cast<long long>(E) * (align - 1) + align;
-  if (R >= (1ll << 31) || capl >= (1ll << 31)) return -1;
-  if (!counts || !offsets || !perm_src || !w_perm) return -1;
-  if (T > 0 && (!topk_ids || !topk_w || !inv_perm)) return -1;
-  if (x && (!x_perm || D <= 0 || D % 8 != 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
-            (reinterpret_cast<uintptr_t>(x_perm) & 15)))
-    return -1;
+  // the same argument rules as moe_route_permute (minus the workspace)
+  if (!basic_sizes_ok(T, K, E, align)) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || !perm_src || !w_perm) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!topk_ids || !topk_w || !inv_perm)) return MOE_ERR_INVALID_ARG;
+  if (x && (!x_perm || D <= 0 || D % 8 != 0 || !aligned16(x) || !aligned16(x_perm)))
+    return MOE_ERR_INVALID_ARG;
   // the counters must fit the fixed array
-  const long long need = static_cast<long long>(E) * route_num_chunks(static_cast<int>(R));
-  if (need > kNoAllocErrWord) return -2;
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return -3;
-  if (major != 10 || minor != 3) return -2;
+  const long long need = static_cast<long long>(E) * route_num_chunks(T * K);
+  if (need > kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
+  const int st = check_device();
+  if (st != MOE_OK) return st;
   cudaError_t e = cudaSuccess;
   int32_t* scratch = noalloc_scratch_for_current_device(&e);
-  if (!scratch) return -3;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the array keeps the previous call's contents: the error word must start at zero
-  // (the chunk counters are fully rewritten by every call)
-  if (cudaMemsetAsync(scratch + kNoAllocErrWord, 0, sizeof(int32_t), s) != cudaSuccess) return -3;
-  const size_t cap = (static_cast<size_t>(R) + static_cast<size_t>(E) * (align - 1) + align - 1) /
-                     align * align;
-  e = launch_route(topk_ids, topk_w, x, T, K, E, D, align, static_cast<int>(cap), counts, offsets,
-                   perm_src, inv_perm, w_perm, x_perm, scratch, scratch + kNoAllocErrWord,
-                   nullptr, s);
-  return e == cudaSuccess ? 0 : -3;
+  if (!scratch) return MOE_ERR_CUDA;
+  // every chunk counter is rewritten by each call before it is read, so nothing needs
+  // clearing; expert ids outside [0, E) are skipped without being reported (no error slot)
+  e = launch_route(topk_ids, topk_w, x, T, K, E, D, align,
+                   static_cast<int>(capacity_of(T, K, E, align)), counts, offsets, perm_src,
+                   inv_perm, w_perm, x_perm, scratch, nullptr, nullptr,
+                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

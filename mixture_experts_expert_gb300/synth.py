@@ -1,8 +1,11 @@
 """Seeded synthetic inputs for the routed MoE expert-MLP layer.
 
-This module only draws inputs; it holds none of the layer's arithmetic (no
-permutation, no expert MLP, no combine, no gradient). Both the CUDA path and
-the CPU oracle consume the arrays it returns, bit for bit.
+This module draws inputs.  It holds none of the expert-MLP layer's arithmetic (no
+permutation, no expert MLP, no combine, no gradient).  It does derive the layer's
+routing input from the drawn logits (``route_from_logits``, plain torch ops): that
+is the input recipe the workloads state, not a reference for the library's own
+router kernel, which the tests check against the oracle's router instead.  Both the
+CUDA path and the CPU oracle consume the arrays it returns, bit for bit.
 
 Recipe (one generator, fixed draw order):
 
@@ -99,7 +102,9 @@ def shape_by_name(name: str) -> MoEShape:
 
 
 def route_from_logits(logits: torch.Tensor, K: int, router: str):
-    """Top-K expert ids (int32) and fp32 router weights from fp32 logits."""
+    """Top-K expert ids (int32) and fp32 router weights from fp32 logits: the routing
+    input of the synthetic workloads (the router step itself is the library's
+    moe_router_topk, checked against the oracle, not against this function)."""
     if router == "softmax":
         probs = torch.softmax(logits.float(), dim=-1)
         # stable descending sort: among equal probabilities the lower index wins

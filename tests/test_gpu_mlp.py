@@ -57,8 +57,12 @@ def run_gpu(inp, T, D, I, E, K, align=128):
     return layer
 
 
-def check_full(inp, T, D, I, E, K, align=128):
+def check_full(inp, T, D, I, E, K, align=128, grad_unit=1.0):
+    """Every output against the oracle.  `grad_unit` (a power of two): the scale dY was
+    drawn at; gradients are compared in that unit (both sides divided by it, exactly), so
+    the absolute bar means the same at every scale of dY."""
     layer = run_gpu(inp, T, D, I, E, K, align)
+    gu = float(grad_unit)
     x, wg, wu, wd, dy, w = (f64(inp[k]) for k in ("x", "w_gate", "w_up", "w_down", "dy", "topk_w"))
     ids = i64(inp["topk_ids"])
     r = oracle.route_permute(ids, w, x, E, align)
@@ -74,12 +78,12 @@ def check_full(inp, T, D, I, E, K, align=128):
     assert_close(layer.y, oracle.moe_forward(x, ids, w, wg, wu, wd), "Y")
     dxp, pg, pu, pd = oracle.expert_mlp_bwd(dy, r["x_perm"], r["perm_src"], r["w_perm"],
                                             r["offsets"], wg, wu, wd, K)
-    assert_close(layer.dx_perm[:used], dxp[:used], "dx_perm")
+    assert_close(f64(layer.dx_perm[:used]) / gu, dxp[:used] / gu, "dx_perm")
     dX, dWg, dWu, dWd = oracle.moe_backward(x, ids, w, wg, wu, wd, dy)
-    assert_close(layer.dx, dX, "dX")
-    assert_close(layer.dw_gate, dWg, "dW_gate")
-    assert_close(layer.dw_up, dWu, "dW_up")
-    assert_close(layer.dw_down, dWd, "dW_down")
+    assert_close(f64(layer.dx) / gu, dX / gu, "dX")
+    assert_close(f64(layer.dw_gate) / gu, dWg / gu, "dW_gate")
+    assert_close(f64(layer.dw_up) / gu, dWu / gu, "dW_up")
+    assert_close(f64(layer.dw_down) / gu, dWd / gu, "dW_down")
     counts = r["counts"]
     for e in np.nonzero(counts == 0)[0]:
         assert bool((layer.dw_gate[e] == 0).all() and (layer.dw_up[e] == 0).all()
@@ -214,14 +218,14 @@ def _sample_experts(counts, rng):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.sweep_shape(1024),
-                                   synth.sweep_shape(2048), synth.sweep_shape(4096),
-                                   synth.sweep_shape(16384), synth.sweep_shape(32768),
-                                   synth.sweep_shape(65536), synth.SKEWED, synth.SKEWED_STEEP,
-                                   synth.LLAMA4_SCOUT, synth.SCOUT_SKEWED], ids=lambda s: s.name)
-def test_full_size_workloads_sampled(shape):
-    s = shape
+def check_sampled(s, dy_scale=1.0):
+    """A full-size workload in the benchmark's launch configuration, compared with the
+    oracle on sampled tokens (Y, dX) and sampled experts (y_perm, dx_perm, dW).  dY is
+    multiplied by `dy_scale` (a power of two, exact in bf16); gradients are compared in
+    that unit."""
     inp_dev = synth.make_inputs(s, device=DEV)
+    if dy_scale != 1.0:
+        inp_dev["dy"] = inp_dev["dy"] * dy_scale
     layer = MoEExpertMLP(s.T, s.K, s.E, s.D, s.I, align=128, device=DEV)
     y = layer.forward(inp_dev["x"], inp_dev["topk_ids"], inp_dev["topk_w"], inp_dev["w_gate"],
                       inp_dev["w_up"], inp_dev["w_down"])
@@ -240,7 +244,8 @@ def test_full_size_workloads_sampled(shape):
     assert_close(f64(y)[tok], y_ref, "Y (sampled tokens)")
     dx_ref = oracle.moe_backward(x[tok], ids[tok], w[tok], wg, wu, wd, dy[tok],
                                  weight_grads=False)[0]
-    assert_close(f64(layer.dx)[tok], dx_ref, "dX (sampled tokens)")
+    gu = float(dy_scale)
+    assert_close(f64(layer.dx)[tok] / gu, dx_ref / gu, "dX (sampled tokens)")
 
     # sampled experts: sorted-row outputs and weight gradients
     r = oracle.route_permute(ids, w, x, s.E, 128)
@@ -253,12 +258,22 @@ def test_full_size_workloads_sampled(shape):
         rows = slice(int(r["offsets"][e]), int(r["offsets"][e + 1]))
         if rows.stop > rows.start:
             assert_close(layer.y_perm[rows], yp[rows], f"y_perm[e={e}]")
-            assert_close(layer.dx_perm[rows], dxp[rows], f"dx_perm[e={e}]")
-        assert_close(layer.dw_gate[e], dwg[e], f"dW_gate[e={e}]")
-        assert_close(layer.dw_up[e], dwu[e], f"dW_up[e={e}]")
-        assert_close(layer.dw_down[e], dwd[e], f"dW_down[e={e}]")
+            assert_close(f64(layer.dx_perm[rows]) / gu, dxp[rows] / gu, f"dx_perm[e={e}]")
+        assert_close(f64(layer.dw_gate[e]) / gu, dwg[e] / gu, f"dW_gate[e={e}]")
+        assert_close(f64(layer.dw_up[e]) / gu, dwu[e] / gu, f"dW_up[e={e}]")
+        assert_close(f64(layer.dw_down[e]) / gu, dwd[e] / gu, f"dW_down[e={e}]")
         if r["counts"][e] == 0:
             assert bool((layer.dw_gate[e] == 0).all() and (layer.dw_down[e] == 0).all())
+    return layer
+
+
+@pytest.mark.parametrize("shape", [synth.QWEN3_30B_A3B, synth.sweep_shape(1024),
+                                   synth.sweep_shape(2048), synth.sweep_shape(4096),
+                                   synth.sweep_shape(16384), synth.sweep_shape(32768),
+                                   synth.sweep_shape(65536), synth.SKEWED, synth.SKEWED_STEEP,
+                                   synth.LLAMA4_SCOUT, synth.SCOUT_SKEWED], ids=lambda s: s.name)
+def test_full_size_workloads_sampled(shape):
+    check_sampled(shape)
 
 
 def test_repeated_calls_are_bitwise_stable():

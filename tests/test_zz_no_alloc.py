@@ -33,7 +33,7 @@ def outputs(T, K, E, D, align, with_x):
                 if with_x else None)
 
 
-def route_both(ids, w, x, E, align):
+def route_both(ids, w, x, E, align, want_ws_error=B.MOE_OK):
     T, K = ids.shape
     D = x.shape[1]
     ref = outputs(T, K, E, D, align, True)
@@ -42,6 +42,7 @@ def route_both(ids, w, x, E, align):
     B.moe_workspace_init(ws)
     B.moe_route_permute(ids, w, x, T, K, E, D, align, ref["counts"], ref["offsets"],
                         ref["perm_src"], ref["inv_perm"], ref["w_perm"], ref["x_perm"], ws)
+    assert B.moe_get_device_error(ws)[0] == want_ws_error
     got = outputs(T, K, E, D, align, True)
     B.moe_route_permute_noalloc(ids, w, x, T, K, E, D, align, got["counts"], got["offsets"],
                                 got["perm_src"], got["inv_perm"], got["w_perm"], got["x_perm"])
@@ -75,3 +76,25 @@ def test_rejects_sizes_beyond_the_fixed_array():
                                       for n in (E, E + 1, B.moe_capacity(T, K, E, 128), T * K)],
                                     torch.zeros(B.moe_capacity(T, K, E, 128), device=DEV), None)
     assert ei.value.status == B.MOE_ERR_UNSUPPORTED
+
+
+def test_no_tokens_with_x_given():
+    """T = 0 with x given: nothing is routed or gathered; counts and offsets are zero and
+    every row is padding, exactly as moe_route_permute leaves them."""
+    E, K, D = 6, 2, 256
+    x = torch.randn(1, D, device=DEV).to(torch.bfloat16)   # non-NULL, never read
+    ids = torch.zeros(0, K, dtype=torch.int32, device=DEV)
+    w = torch.zeros(0, K, dtype=torch.float32, device=DEV)
+    route_both(ids, w, x, E, 128)
+
+
+def test_expert_ids_outside_the_range_are_skipped():
+    """Slots whose expert id lies outside [0, E) reach no row in either entry point (the
+    workspace version also reports them); every other output agrees bit for bit."""
+    T, K, E, D = 500, 3, 9, 256
+    ids, w = synth.random_routing(T, K, E, seed=11, device=DEV)
+    ids[7, 1] = E
+    ids[100, 0] = -1
+    ids[333, 2] = 1 << 20
+    x = torch.randn(T, D, device=DEV).to(torch.bfloat16)
+    route_both(ids, w, x, E, 128, want_ws_error=B.MOE_ERR_BAD_INDEX)
