@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import PerExpert, assert_close, f64, i64
+from helpers import MAX_ABS_TOL, REL_FRO_TOL, PerExpert, assert_close, f64, i64
 from mixture_experts_expert_gb300 import binding as B
 from mixture_experts_expert_gb300 import build as Bld
 from mixture_experts_expert_gb300 import synth
@@ -274,6 +274,57 @@ def check_sampled(s, dy_scale=1.0):
                                    synth.LLAMA4_SCOUT, synth.SCOUT_SKEWED], ids=lambda s: s.name)
 def test_full_size_workloads_sampled(shape):
     check_sampled(shape)
+
+
+def test_qwen3_30b_a3b_full_tensors():
+    """The headline workload (Qwen3-30B-A3B shape, T = 8192) in the benchmark's launch
+    configuration, compared with the oracle on every element: Y, y_perm, dx_perm, dX and all
+    3 x 128 weight-gradient matrices, each as one tensor (relative Frobenius error over the
+    whole tensor, max-abs over all its elements).  The oracle runs expert by expert, 16
+    experts at a time, to bound host memory."""
+    s = synth.QWEN3_30B_A3B
+    inp_dev = synth.make_inputs(s, device=DEV)
+    layer = MoEExpertMLP(s.T, s.K, s.E, s.D, s.I, align=128, device=DEV)
+    y = layer.forward(inp_dev["x"], inp_dev["topk_ids"], inp_dev["topk_w"], inp_dev["w_gate"],
+                      inp_dev["w_up"], inp_dev["w_down"])
+    layer.backward(inp_dev["dy"], inp_dev["w_gate"], inp_dev["w_up"], inp_dev["w_down"])
+    torch.cuda.synchronize()
+    assert layer.device_error()[0] == B.MOE_OK
+
+    x, dy, w = f64(inp_dev["x"]), f64(inp_dev["dy"]), f64(inp_dev["topk_w"])
+    ids = i64(inp_dev["topk_ids"])
+    wg, wu, wd = (PerExpert(inp_dev[k]) for k in ("w_gate", "w_up", "w_down"))
+    r = oracle.route_permute(ids, w, x, s.E, 128)
+    assert np.array_equal(i64(layer.offsets), r["offsets"])
+    used = int(r["offsets"][-1])
+    y_perm = oracle.expert_mlp_fwd(r["x_perm"], wg, wu, wd, r["offsets"])
+    assert_close(layer.y_perm[:used], y_perm[:used], "y_perm")
+    assert_close(y, oracle.combine(y_perm, r["inv_perm"], w, s.T, s.K), "Y")
+    del y_perm
+
+    dx_perm = np.zeros(r["x_perm"].shape)
+    stats = {n: [0.0, 0.0, 0.0] for n in ("dW_gate", "dW_up", "dW_down")}   # err^2, ref^2, max
+    for e0 in range(0, s.E, 16):
+        batch = list(range(e0, min(s.E, e0 + 16)))
+        dxp, dwg, dwu, dwd = oracle.expert_mlp_bwd(dy, r["x_perm"], r["perm_src"], r["w_perm"],
+                                                   r["offsets"], wg, wu, wd, s.K, experts=batch)
+        for e in batch:
+            rows = slice(int(r["offsets"][e]), int(r["offsets"][e + 1]))
+            dx_perm[rows] = dxp[rows]
+            for name, got, ref in (("dW_gate", layer.dw_gate[e], dwg[e]),
+                                   ("dW_up", layer.dw_up[e], dwu[e]),
+                                   ("dW_down", layer.dw_down[e], dwd[e])):
+                diff = f64(got) - ref
+                st = stats[name]
+                st[0] += float(np.sum(diff * diff))
+                st[1] += float(np.sum(ref * ref))
+                st[2] = max(st[2], float(np.max(np.abs(diff))))
+    for name, (e2, r2, mx) in stats.items():
+        rel = (e2 ** 0.5) / (r2 ** 0.5)
+        assert mx <= MAX_ABS_TOL and rel <= REL_FRO_TOL, \
+            f"{name}: max abs {mx:.3e}, rel fro {rel:.3e}"
+    assert_close(layer.dx_perm[:used], dx_perm[:used], "dx_perm")
+    assert_close(layer.dx, oracle.combine(dx_perm, r["inv_perm"], None, s.T, s.K), "dX")
 
 
 def test_repeated_calls_are_bitwise_stable():
