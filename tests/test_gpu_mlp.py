@@ -120,10 +120,11 @@ def test_coarser_padding(align):
 @pytest.mark.parametrize("I", [256, 384])
 def test_tail_tile_sizes(I):
     """Experts whose last row tile has 1, 31, 32, 33, 127, 128 real rows (one tile), 129
-    (two tiles) and 300 (three): every odd last tile is computed transposed over its real
-    rows rounded up to 32, the rest of it written as zeros.  With I = 384 the dA GEMM has
-    128-column tiles and runs those tiles with an idle CTA half instead."""
-    counts = [1, 31, 32, 33, 127, 128, 129, 300, 0]
+    (two tiles), 300, 352, 353 (three) and 513, 640 (five): every odd last tile is computed
+    transposed over its real rows rounded up to 32, the rest of it written as zeros.  With
+    I = 384 the dA GEMM has 128-column tiles and runs those tiles with an idle CTA half
+    instead."""
+    counts = [1, 31, 32, 33, 127, 128, 129, 300, 0, 352, 353, 513, 640]
     E, K, D = len(counts), 1, 256
     T = sum(counts)
     ids = torch.cat([torch.full((c, 1), e, dtype=torch.int32) for e, c in enumerate(counts)])
