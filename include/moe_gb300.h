@@ -12,9 +12,10 @@
  *   - All tensors are dense and row-major.  bf16 tensors are passed as raw 16-bit
  *     storage (moe_bf16_t).  Sizes are element counts.
  *   - Device pointers point to memory of the current CUDA device.  The library
- *     allocates nothing and never synchronises the host (except
+ *     allocates no memory and never synchronises the host (except
  *     moe_get_device_error and moe_timing_collect); every call enqueues its kernels
- *     on `stream` (a cudaStream_t, NULL = legacy default stream) and returns.
+ *     on `stream` (a cudaStream_t, NULL = legacy default stream) and returns
+ *     (moe_expert_mlp_bwd also uses a side stream of its own, joined before it returns).
  *   - The caller owns every buffer.  Buffers must not alias unless stated.
  *   - Arguments are validated on the host before anything is launched; a failed
  *     check returns a negative moe_status_t and launches nothing.  Conditions only
@@ -38,7 +39,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 4
+#define MOE_ABI_VERSION 5
 
 typedef uint16_t moe_bf16_t;
 
@@ -178,7 +179,15 @@ int moe_combine(const moe_bf16_t* src_perm, const int32_t* inv_perm, const float
  *   rows is gathered from it (each token row is read K times, mostly from cache) instead
  *   of being read from x_perm.  Outputs (device): dx_perm [cap,D] bf16 (rows < offsets[E]),
  *   dw_gate [E,D,I] fp32, dw_up [E,D,I] fp32, dw_down [E,I,D] fp32 (fully overwritten).
- * Reduce dx_perm to tokens with moe_combine(dx_perm, inv_perm, NULL, ...).
+ *   inv_perm [T*K] int32 (moe_route_permute's) and dx [T,D] bf16 (device), both or neither:
+ *   when given, the call also reduces dx_perm to tokens, dx = moe_combine(dx_perm,
+ *   inv_perm, NULL) bit for bit, beside its weight-gradient GEMMs; when NULL, reduce
+ *   dx_perm with moe_combine(dx_perm, inv_perm, NULL, ...) afterwards.
+ * Concurrency: with dx given, the dx reduction runs on a second, low-priority stream of
+ * the library's own, beside the weight-gradient GEMMs (its blocks share each SM with a GEMM
+ * CTA); that stream forks from and joins back into `stream` within the call, so the call
+ * behaves as if everything ran on `stream`, also inside a stream capture.  The first such
+ * call on a device creates that stream and its events: make it before any capture.
  * Needs D % 256 == 0, I % 128 == 0, align % 128 == 0.
  */
 int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x, const moe_bf16_t* x_perm,
@@ -187,7 +196,7 @@ int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x, const moe_bf16
                        const moe_bf16_t* w_gate, const moe_bf16_t* w_up,
                        const moe_bf16_t* w_down, int T, int K, int E, int D, int I, int align,
                        moe_bf16_t* dx_perm, float* dw_gate, float* dw_up, float* dw_down,
-                       void* workspace, void* stream);
+                       const int32_t* inv_perm, moe_bf16_t* dx, void* workspace, void* stream);
 
 /* ---- router step ------------------------------------------------------------
  * The pages have the forward's final combine apply the router weights ("LigerMoE

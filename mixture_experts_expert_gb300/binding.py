@@ -57,7 +57,7 @@ _SIGS = {
     "moe_expert_mlp_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_expert_mlp_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
-                                _P, _P, _P, _P, _P, _P]),
+                                _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_get_device_error": (_I, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I), _P]),
     "moe_route_permute_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                        _P]),
@@ -199,7 +199,8 @@ def moe_combine(src_perm, inv_perm, topk_w, T, K, D, out, stream=None):
 
 def moe_expert_mlp_bwd(dy, x, x_perm, perm_src, w_perm, offsets, counts, w_gate, w_up, w_down,
                        T, K, E, D, I, align, dx_perm, dw_gate, dw_up, dw_down, workspace,
-                       stream=None):
+                       stream=None, inv_perm=None, dx=None):
+    """With inv_perm and dx the call also reduces dx_perm to tokens into dx."""
     bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
     st = lib().moe_expert_mlp_bwd(
         _ptr(dy, bf, "dy", T == 0), _ptr(x, bf, "x", True), _ptr(x_perm, bf, "x_perm"), _ptr(perm_src, i32, "perm_src"),
@@ -207,7 +208,8 @@ def moe_expert_mlp_bwd(dy, x, x_perm, perm_src, w_perm, offsets, counts, w_gate,
         _ptr(counts, i32, "counts", True), _ptr(w_gate, bf, "w_gate"),
         _ptr(w_up, bf, "w_up"), _ptr(w_down, bf, "w_down"), T, K, E, D, I, align,
         _ptr(dx_perm, bf, "dx_perm"), _ptr(dw_gate, f32, "dw_gate"), _ptr(dw_up, f32, "dw_up"),
-        _ptr(dw_down, f32, "dw_down"), _ptr(workspace, name="workspace"), _stream(stream))
+        _ptr(dw_down, f32, "dw_down"), _ptr(inv_perm, i32, "inv_perm", True),
+        _ptr(dx, bf, "dx", True), _ptr(workspace, name="workspace"), _stream(stream))
     _check("moe_expert_mlp_bwd", st)
 
 

@@ -90,6 +90,52 @@ static const DevFacts* dev_facts() {
   return &f;
 }
 
+// ------------------------------------------------------------------ side stream
+// The backward reduces dx_perm to tokens (when the caller asks it to) on a second stream of
+// the library's own, beside its weight-gradient GEMMs: the reduction's blocks fit on an SM
+// next to a GEMM CTA (no shared memory, few registers) and use HBM bandwidth the
+// latency-bound GEMMs leave idle.  The stream has the lowest priority, so that the GEMMs'
+// CTAs are placed first.  (Running the fp16 operand copies beside the token-row GEMMs the
+// same way measured slower: those GEMMs lost more time than the copies took.)  One side
+// stream and three events per device, created by the first backward on it; the enqueue
+// sequence of a backward holds the mutex, so concurrent callers cannot interleave their
+// event records.
+struct SideStream {
+  bool init = false;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, spare = nullptr;
+};
+static SideStream g_side[64];
+static std::mutex g_side_mu;
+
+static SideStream* side_stream(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  SideStream& ss = g_side[dev];
+  if (!ss.init) {
+    int least = 0, greatest = 0;
+    if ((*err = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess ||
+        (*err = cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, least)) != cudaSuccess)
+      return nullptr;
+    cudaEvent_t* evs[3] = {&ss.fork, &ss.join, &ss.spare};
+    for (cudaEvent_t* e : evs)
+      if ((*err = cudaEventCreateWithFlags(e, cudaEventDisableTiming)) != cudaSuccess) return nullptr;
+    ss.init = true;
+  }
+  return &ss;
+}
+
+// Makes `to` wait for the work enqueued on `from` so far.
+static cudaError_t stream_after(cudaStream_t to, cudaStream_t from, cudaEvent_t ev) {
+  cudaError_t e = cudaEventRecord(ev, from);
+  return e == cudaSuccess ? cudaStreamWaitEvent(to, ev, 0) : e;
+}
+
 // ------------------------------------------------------------------ tensor maps
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -457,6 +503,21 @@ MOE_EXPORT int moe_expert_mlp_fwd(const moe_bf16_t* x_perm, const moe_bf16_t* w_
   return to_status(e);
 }
 
+// The dx reduction the backward runs on its side stream (none when ss is null).
+struct SideWork {
+  SideStream* ss;
+  const moe_bf16_t* dx_perm;
+  const int32_t* inv_perm;
+  moe_bf16_t* dx;
+  int T, K, D;
+};
+
+static int bwd_weight_grads(const int32_t* offsets, const int32_t* counts, int* dw_prefix,
+                            int* err, const uint32_t* maxabs, int E, int D, int I, uint64_t cap,
+                            int chunk, void* act, void* act_lo, void* dh16, void* dh16_lo,
+                            moe_bf16_t* xp16, moe_bf16_t* dyp16, float* dw_gate, float* dw_up,
+                            float* dw_down, int num_sms, const SideWork& side, cudaStream_t s);
+
 MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
                                   const moe_bf16_t* x_perm,
                                   const int32_t* perm_src, const float* w_perm,
@@ -464,7 +525,8 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
                                   const moe_bf16_t* w_gate,
                                   const moe_bf16_t* w_up, const moe_bf16_t* w_down, int T, int K,
                                   int E, int D, int I, int align, moe_bf16_t* dx_perm,
-                                  float* dw_gate, float* dw_up, float* dw_down, void* workspace,
+                                  float* dw_gate, float* dw_up, float* dw_down,
+                                  const int32_t* inv_perm, moe_bf16_t* dx, void* workspace,
                                   void* stream) {
   if (!basic_sizes_ok(T, K, E, align)) return MOE_ERR_INVALID_ARG;
   if (!gemm_shape_ok(D, I, align)) return MOE_ERR_UNSUPPORTED;
@@ -475,9 +537,20 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
       !aligned16(dx_perm) || !aligned16(dw_gate) || !aligned16(dw_up) || !aligned16(dw_down) ||
       !aligned16(workspace) || (dy && !aligned16(dy)) || (x && !aligned16(x)))
     return MOE_ERR_INVALID_ARG;
+  // optional: the reduction of dx_perm to tokens, done inside this call
+  if ((dx == nullptr) != (inv_perm == nullptr) || (dx && !aligned16(dx)))
+    return MOE_ERR_INVALID_ARG;
   int st = check_device();
   if (st != MOE_OK) return st;
   const DevFacts* f = dev_facts();
+  std::unique_lock<std::mutex> side_lock(g_side_mu, std::defer_lock);
+  SideStream* ss = nullptr;
+  if (dx && T > 0) {
+    side_lock.lock();
+    cudaError_t se = cudaSuccess;
+    ss = side_stream(&se);
+    if (!ss) return MOE_ERR_CUDA;
+  }
   const WsLayout L = ws_layout(T, K, E, D, I, align);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const uint64_t cap = capacity_of(T, K, E, align);
@@ -570,8 +643,24 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
     e = launch_gemm_kind<GemmKind::Dx>(xg, pairs_max * xg.n_tiles, f->num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // the dx reduction to tokens (when asked for) on the side stream, beside the
+  // weight-gradient GEMMs; joined back before the call returns
+  const SideWork side{ss, dx_perm, inv_perm, dx, T, K, D};
+  return bwd_weight_grads(offsets, counts, dw_prefix, err, maxabs, E, D, I, cap, chunk, act,
+                          act_lo, dh16, dh16_lo, xp16, dyp16, dw_gate, dw_up, dw_down, f->num_sms,
+                          side, s);
+}
 
-  // 4. weight gradients (fp16 operands, fp32 accumulate and output)
+// Step 4 of the backward: the weight gradients (fp16 operands, fp32 accumulate and output).
+static int bwd_weight_grads(const int32_t* offsets, const int32_t* counts, int* dw_prefix,
+                            int* err, const uint32_t* maxabs, int E, int D, int I, uint64_t cap,
+                            int chunk, void* act, void* act_lo, void* dh16, void* dh16_lo,
+                            moe_bf16_t* xp16, moe_bf16_t* dyp16, float* dw_gate, float* dw_up,
+                            float* dw_down, int num_sms, const SideWork& side, cudaStream_t s) {
+  const uint64_t ED = static_cast<uint64_t>(E) * D, EI = static_cast<uint64_t>(E) * I;
+  cudaError_t e;
+  bool ok;
+
   e = launch_dw_prep(offsets, E, chunk, dw_prefix, dw_gate, dw_up, dw_down, D, I, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int max_chunks = E + static_cast<int>(cap / chunk) + 1;
@@ -589,7 +678,7 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   g.n_tiles = (2 * I) / 256;
   {
     LaunchScope ls(kKGemmDwGU, s);
-    e = launch_gemm_kind<GemmKind::DwGU>(g, max_chunks * g.m_tiles * g.n_tiles, f->num_sms, s);
+    e = launch_gemm_kind<GemmKind::DwGU>(g, max_chunks * g.m_tiles * g.n_tiles, num_sms, s);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   GemmParams d{};
@@ -604,11 +693,23 @@ MOE_EXPORT int moe_expert_mlp_bwd(const moe_bf16_t* dy, const moe_bf16_t* x,
   if (!ok) return MOE_ERR_CUDA;
   d.m_tiles = I / 128;
   d.n_tiles = D / 256;
-  {
+  if (!side.ss) {
     LaunchScope ls(kKGemmDwD, s);
-    e = launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, f->num_sms, s);
+    return to_status(
+        launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, num_sms, s));
   }
-  return to_status(e);
+  // the dx reduction on the side stream, beside the dW_down GEMM (it only needs the dX
+  // GEMM, which is done by now); every exit from here joins the side stream back
+  SideStream* ss = side.ss;
+  if (stream_after(ss->s, s, ss->fork) != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_combine(side.dx_perm, side.inv_perm, nullptr, side.T, side.K, side.D, side.dx,
+                     ss->s);
+  if (e == cudaSuccess) {
+    LaunchScope ls(kKGemmDwD, s);
+    e = launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, num_sms, s);
+  }
+  const cudaError_t je = stream_after(s, ss->s, ss->join);
+  return e != cudaSuccess ? MOE_ERR_CUDA : to_status(je);
 }
 
 MOE_EXPORT int moe_tuning_get(int T, int K, int E, int D, int I, moe_tuning_t* out,

@@ -5,7 +5,8 @@ entry points together.
 Router (optional): moe_router_topk (logits -> topk_ids, topk_w); after the backward,
 moe_router_weight_grad + moe_router_backward (-> d_logits).
 Forward:  moe_route_permute -> moe_expert_mlp_fwd -> moe_combine(topk_w)
-Backward: moe_expert_mlp_bwd -> moe_combine(NULL)   (reduces routed dX to tokens)
+Backward: moe_expert_mlp_bwd (which also reduces the routed dX to tokens; or, with
+          reduce_in_backward=False, moe_expert_mlp_bwd -> moe_combine(NULL))
 
 Buffer shapes are fixed by (T, K, E, D, I, align), so a forward/backward pair can
 be captured once in a CUDA graph and replayed with new inputs and routings.
@@ -20,12 +21,16 @@ from . import binding as B
 class MoEExpertMLP:
     """`skip_padding`: pass the routing's per-expert counts to the GEMMs so that they
     compute only the real rows of each expert's last row tile (rounded up to 32); off,
-    every padded row is computed.  The results are the same either way."""
+    every padded row is computed.  `reduce_in_backward`: moe_expert_mlp_bwd reduces the
+    routed dX to tokens itself, beside its weight-gradient GEMMs; off, a separate
+    moe_combine call does it afterwards.  The results are the same bit for bit."""
 
     def __init__(self, T: int, K: int, E: int, D: int, I: int, align: int = 128,
-                 device: str | torch.device = "cuda", skip_padding: bool = True):
+                 device: str | torch.device = "cuda", skip_padding: bool = True,
+                 reduce_in_backward: bool = True):
         self.T, self.K, self.E, self.D, self.I, self.align = T, K, E, D, I, align
         self.skip_padding = skip_padding
+        self.reduce_in_backward = reduce_in_backward
         dev = torch.device(device)
         self.device = dev
         self.cap = B.moe_capacity(T, K, E, align)
@@ -70,11 +75,14 @@ class MoEExpertMLP:
         """(dX [T,D] bf16, dW_gate [E,D,I] f32, dW_up [E,D,I] f32, dW_down [E,I,D] f32)
         of L = sum(Y * dy), for the routing of the last forward."""
         T, K, E, D, I, a = self.T, self.K, self.E, self.D, self.I, self.align
+        dx = self.dx if dx_out is None else dx_out
+        fused = self.reduce_in_backward and T > 0
         B.moe_expert_mlp_bwd(dy, self._x, self.x_perm, self.perm_src, self.w_perm, self.offsets,
                              self._counts(), w_gate, w_up, w_down, T, K, E, D, I, a, self.dx_perm,
-                             self.dw_gate, self.dw_up, self.dw_down, self.workspace, stream)
-        dx = self.dx if dx_out is None else dx_out
-        B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, dx, stream)
+                             self.dw_gate, self.dw_up, self.dw_down, self.workspace, stream,
+                             inv_perm=self.inv_perm if fused else None, dx=dx if fused else None)
+        if not fused:
+            B.moe_combine(self.dx_perm, self.inv_perm, None, T, K, D, dx, stream)
         return dx, self.dw_gate, self.dw_up, self.dw_down
 
     def route(self, logits, router="softmax", stream=None):

@@ -48,7 +48,7 @@ def test_library_is_sm103a_only():
 
 
 def test_abi_version_and_status_strings(lib):
-    assert B.moe_abi_version() == 4
+    assert B.moe_abi_version() == 5
     assert B.moe_status_string(0) == "ok"
     assert "invalid" in B.moe_status_string(-1)
     assert B.moe_status_string(12345) == "unknown status"
@@ -81,7 +81,7 @@ def test_invalid_sizes_rejected_on_host(lib):
                               nul)
     assert st == B.MOE_ERR_UNSUPPORTED
     st = L.moe_expert_mlp_bwd(nul, nul, nul, nul, nul, nul, nul, nul, nul, nul, 8, 2, 4, 256,
-                              96, 128, nul, nul, nul, nul, nul, nul)
+                              96, 128, nul, nul, nul, nul, nul, nul, nul, nul)
     assert st == B.MOE_ERR_UNSUPPORTED
     # null buffers are rejected
     st = L.moe_expert_mlp_fwd(nul, nul, nul, nul, nul, nul, 8, 2, 4, 256, 128, 128, nul, nul,

@@ -86,3 +86,19 @@ def test_expired_wait_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     for got, want in zip(outputs(layer), outputs(ref)):
         assert torch.equal(got, want)
+
+
+def test_reduction_inside_backward_matches_separate_combine():
+    """moe_expert_mlp_bwd reducing dx_perm to tokens itself (on its side stream, beside the
+    weight-gradient GEMMs) gives exactly what a separate moe_combine call gives."""
+    T, D, I, E, K = (SHAPE[k] for k in ("T", "D", "I", "E", "K"))
+    t = {k: v.to(DEV) for k, v in random_layer(T, D, I, E, K, seed=27).items()}
+    runs = []
+    for fused in (True, False):
+        layer = MoEExpertMLP(T, K, E, D, I, device=DEV, reduce_in_backward=fused)
+        step(layer, t)
+        torch.cuda.synchronize()
+        assert layer.device_error()[0] == B.MOE_OK
+        runs.append(outputs(layer))
+    for a, b in zip(*runs):
+        assert torch.equal(a, b)
