@@ -52,12 +52,15 @@ def gemm_bytes(s):
 def movement_bytes(s):
     """Algorithmic bytes per launch of the HBM-bound kernels (what each must read and
     write at the minimum): permute (x rows in, sorted rows out, slot ids and weights),
-    combine (sorted rows in, token rows out, inverse permutation and weights) and the
+    combine (sorted rows in, token rows out, inverse permutation and weights), the
+    backward's dX reduction (the same without weights; it runs beside the dW_down GEMM,
+    so its time there is shared time) and the
     backward's row preparation (dY and x rows in; dY_perm, its fp16 copy and the fp16
     copy of x_perm out)."""
     T, R, D = s.T, s.R, s.D
     return {"gather_x": T * D * 2 + R * D * 2 + 8 * R,
             "combine": R * D * 2 + 8 * R + T * D * 2,
+            "combine_dx": R * D * 2 + 4 * R + T * D * 2,
             "bwd_prep_rows": 2 * T * D * 2 + 3 * R * D * 2 + 4 * R}
 
 

@@ -60,6 +60,7 @@ enum KernelId : int {
   kKRouterBwd,
   kKRouteFused,
   kKBwdPrepPad,
+  kKCombineDx,     // the backward's dX reduction (the combine kernel, run inside the backward)
   kNumKernelIds
 };
 
@@ -155,7 +156,8 @@ cudaError_t launch_bwd_prep_rows(const uint16_t* dy, const uint16_t* x, const ui
                                  cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
-                           int T, int K, int D, uint16_t* out, cudaStream_t s);
+                           int T, int K, int D, uint16_t* out, cudaStream_t s,
+                           int kernel_id = kKCombine);
 
 cudaError_t launch_dw_prep(const int32_t* offsets, int E, int chunk_rows, int* dw_prefix,
                            float* dw_gate, float* dw_up, float* dw_down, int D, int I,

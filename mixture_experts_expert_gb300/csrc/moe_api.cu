@@ -17,7 +17,7 @@ static const char* const kKernelNames[kNumKernelIds] = {
     "route_count", "route_scan", "route_scatter", "gather_x",   "gemm_gateup_swiglu",
     "gemm_down",   "combine",    "bwd_prep_rows", "gemm_dA",    "gemm_bwd_gateup",
     "gemm_dx",     "dw_prep",    "gemm_dw_gateup", "gemm_dw_down", "router_topk",
-    "router_weight_grad", "router_backward", "route_permute", "bwd_prep_pad"};
+    "router_weight_grad", "router_backward", "route_permute", "bwd_prep_pad", "combine_dx"};
 
 const char* kernel_name(int id) {
   return (id >= 0 && id < kNumKernelIds) ? kKernelNames[id] : nullptr;
@@ -703,7 +703,7 @@ static int bwd_weight_grads(const int32_t* offsets, const int32_t* counts, int* 
   SideStream* ss = side.ss;
   if (stream_after(ss->s, s, ss->fork) != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_combine(side.dx_perm, side.inv_perm, nullptr, side.T, side.K, side.D, side.dx,
-                     ss->s);
+                     ss->s, kKCombineDx);
   if (e == cudaSuccess) {
     LaunchScope ls(kKGemmDwD, s);
     e = launch_gemm_kind<GemmKind::DwD>(d, max_chunks * d.m_tiles * d.n_tiles, num_sms, s);

@@ -799,10 +799,10 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ sr
 }
 
 cudaError_t launch_combine(const uint16_t* src_perm, const int32_t* inv_perm, const float* w,
-                           int T, int K, int D, uint16_t* out, cudaStream_t s) {
+                           int T, int K, int D, uint16_t* out, cudaStream_t s, int kernel_id) {
   if (T == 0) return cudaSuccess;
   const int blocks = (T + 7) / 8;
-  LaunchScope ls(kKCombine, s);
+  LaunchScope ls(kernel_id, s);
   k_combine<<<blocks, 256, 0, s>>>(src_perm, inv_perm, w, T, K, D, out);
   return cudaGetLastError();
 }
