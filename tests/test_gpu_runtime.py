@@ -4,7 +4,9 @@
   new routing reproduces eager execution bit for bit (launch shapes depend only on the
   sizes, never on the routing);
 * a grouped GEMM whose waits run out reports MOE_ERR_DEVICE_TIMEOUT through the device
-  error word instead of hanging, and the context stays usable afterwards.
+  error word instead of hanging, and the context stays usable afterwards;
+* the backward's in-call dX reduction equals a separate moe_combine, and two layers
+  driven from two host threads on two streams at once give what each gives alone.
 (Values outside the range of the backward's scaled fp16 operands: test_gpu_scales.py.)
 """
 import pytest
@@ -102,3 +104,48 @@ def test_reduction_inside_backward_matches_separate_combine():
         runs.append(outputs(layer))
     for a, b in zip(*runs):
         assert torch.equal(a, b)
+
+
+def test_concurrent_layers_on_two_streams_and_threads():
+    """Two host threads drive two layers on two CUDA streams at once, each backward
+    forking the library's side stream for its dX reduction: every result equals the same
+    layer run alone, bit for bit (the side stream is shared, its use serialised per call,
+    and each call joins it back into its own stream)."""
+    import threading
+
+    T, D, I, E, K = (SHAPE[k] for k in ("T", "D", "I", "E", "K"))
+    inputs = [{k: v.to(DEV) for k, v in random_layer(T, D, I, E, K, seed=s).items()}
+              for s in (28, 29)]
+    want = []
+    for t in inputs:
+        layer = MoEExpertMLP(T, K, E, D, I, device=DEV)
+        step(layer, t)
+        torch.cuda.synchronize()
+        want.append(outputs(layer))
+
+    layers = [MoEExpertMLP(T, K, E, D, I, device=DEV) for _ in inputs]
+    streams = [torch.cuda.Stream() for _ in inputs]
+    errors = []
+
+    def run(i):
+        try:
+            with torch.cuda.stream(streams[i]):
+                for _ in range(5):
+                    step(layers[i], inputs[i])
+            streams[i].synchronize()
+        except Exception as e:   # reported below, on the main thread
+            errors.append(e)
+
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(inputs))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for layer, ref in zip(layers, want):
+        assert layer.device_error()[0] == B.MOE_OK
+        for got, exp in zip(outputs(layer), ref):
+            assert torch.equal(got, exp)
